@@ -1,0 +1,39 @@
+"""CPU float64 oracle for packed variable-length (THD) attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this package: only
+``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may call it. It shares no code, headers, tables or helpers with
+the CUDA path under ``bwd_packed_varlen_gb300/``.
+
+Every function is the plain definition of scaled-dot-product attention written out
+per sequence and per key/value head group, in numpy float64, with no tiling, no
+online softmax and no fusion. The pages this follows (TransformerEngine issues on
+packed-sequence attention) fix:
+
+* real ``cu_seqlens_q/kv`` drive the masks and padded ``cu_seqlens_*_padded`` drive
+  the memory offsets; the output keeps the padded layout (issue #2892, "Expected
+  Behavior", items 1-3);
+* GQA maps query head h to key/value head h // (hq // hkv) (issue #3216,
+  ``fp32_reference`` with ``repeat_interleave``);
+* the causal mask is the upper-left triangle, key j visible to query i iff j <= i
+  (issue #3216, ``torch.triu(..., 1)`` filled with -inf);
+* rows that hold no token of any sequence get exactly-zero gradients (issue #2448,
+  "Expected behavior": the first 4 tokens of dk/dv are zero when the first query
+  sequence is empty).
+
+Parity status of each function is stated in its docstring; all are pinned by the
+``-m "not gpu"`` tests in ``tests/test_oracle.py``.
+"""
+
+from .attention import (  # noqa: F401
+    MASK_PADDING,
+    MASK_PADDING_CAUSAL,
+    seq_spans,
+    attn_group_fwd_bwd,
+    attn_group_bwd_given,
+    attn_fwd_thd,
+    attn_bwd_thd,
+    attn_fwd_bwd_thd,
+    valid_row_masks,
+    fwd_bwd_flops,
+)

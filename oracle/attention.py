@@ -1,0 +1,283 @@
+"""Plain float64 scaled-dot-product attention over packed (THD) sequences.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the CUDA path never imports it.
+
+Notation follows the TransformerEngine pages this oracle restates:
+
+* ``q, out, dout, dq`` are ``[T_q, hq, d]``; ``k, v, dk, dv`` are ``[T_kv, hkv, d]``;
+  ``lse`` is ``[T_q, hq]`` (issue #2448, reproduction script: THD tensors
+  ``(seqlen, heads, dim)`` and the softmax aux tensor ``(seqlen, hq, 1)``).
+* Sequence b occupies rows ``cu_*_padded[b] .. cu_*_padded[b+1]`` of its tensor and
+  holds ``cu_*[b+1] - cu_*[b]`` real tokens at the front of that span (issue #2892,
+  "Expected Behavior": real boundaries mask, padded boundaries index memory).
+* Query head h reads key/value head ``h // G`` with ``G = hq // hkv`` (issue #3216,
+  ``fp32_reference``: ``repeat_interleave`` of K/V over the group), so dK/dV of a
+  key/value head are sums over the G query heads of its group.
+* ``attn_scale`` multiplies ``q k^T`` inside the softmax (issue #2448 passes
+  ``attn_scale=0.1``; issue #3216 divides by sqrt(d)); ``lse`` is the natural log of
+  the softmax denominator of the *scaled* scores.
+* ``padding_causal`` keeps key j for query i iff ``j <= i`` (upper-left alignment,
+  issue #3216 ``torch.triu(ones, 1)`` masked to -inf).
+
+Readings where the pages are silent (each is listed in the design doc as well):
+
+* A valid query whose sequence has no valid key gets ``out = 0``, ``lse = -inf`` and
+  ``dq = 0`` (empty-sum convention).
+* Every row that is not a real token (pad slots, tails, rows of empty sequences) is
+  exactly 0 in ``out, dq`` and ``lse``; key/value rows that are not real tokens, or
+  that no valid query sees, are exactly 0 in ``dk, dv``.
+* The backward entry takes ``out`` and ``lse`` as inputs, as TransformerEngine's
+  ``fused_attn_bwd`` does (issue #2448 passes ``out`` and ``[lse, rng]``), and forms
+  ``P = exp(S - lse)`` and ``D = rowsum(dout * out)`` from them.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+MASK_PADDING = 1
+MASK_PADDING_CAUSAL = 2
+
+_MASKS = {MASK_PADDING: False, MASK_PADDING_CAUSAL: True,
+          "padding": False, "padding_causal": True}
+
+
+def _is_causal(mask_type) -> bool:
+    if mask_type not in _MASKS:
+        raise ValueError(f"unknown mask_type {mask_type!r}")
+    return _MASKS[mask_type]
+
+
+def seq_spans(cu_seqlens, cu_seqlens_padded):
+    """Per sequence ``(offset, real_length)``: offset from the padded prefix sums,
+    length from the real ones (issue #2892, "Expected Behavior", items 1-2)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cp = np.asarray(cu_seqlens_padded, dtype=np.int64)
+    if cu.shape != cp.shape or cu.ndim != 1 or cu.size < 2:
+        raise ValueError("cu_seqlens and cu_seqlens_padded must both be [B+1]")
+    lens = np.diff(cu)
+    plens = np.diff(cp)
+    if np.any(lens < 0) or np.any(lens > plens):
+        raise ValueError("real lengths must be >= 0 and <= padded lengths")
+    return [(int(cp[b]), int(lens[b])) for b in range(lens.size)]
+
+
+def _scores(qh, kg, scale, causal):
+    """S = scale * q k^T for one query head, -inf where the mask removes a key."""
+    s = scale * (qh @ kg.T)
+    if causal:
+        lq, lk = s.shape
+        s[np.arange(lk)[None, :] > np.arange(lq)[:, None]] = -np.inf
+    return s
+
+
+def attn_group_fwd_bwd(qg, kg, vg, dog, scale, causal):
+    """Forward and exact gradient for one sequence and one key/value head group.
+
+    ``qg, dog``: ``[Lq, G, d]``; ``kg, vg``: ``[Lk, d]``. Returns
+    ``(out [Lq,G,d], lse [Lq,G], dq [Lq,G,d], dk [Lk,d], dv [Lk,d])``.
+
+    Forward is the softmax-attention definition (issue #3216 ``fp32_reference``:
+    ``softmax(q k^T / sqrt(d)) v`` with the causal triangle). Backward is the
+    gradient of ``sum(dout * out)`` (issues #3333 and #3216 obtain their reference
+    gradients by autograd of this loss): ``dV = P^T dO``, ``dP = dO V^T``,
+    ``D_i = sum_j P_ij dP_ij``, ``dS = P (dP - D)``, ``dQ = scale dS K``,
+    ``dK = scale dS^T Q``, summed over the G query heads for dK and dV.
+    Parity: pinned (finite differences, torch autograd, closed forms, invariants).
+    """
+    qg = np.asarray(qg, dtype=np.float64)
+    kg = np.asarray(kg, dtype=np.float64)
+    vg = np.asarray(vg, dtype=np.float64)
+    dog = np.asarray(dog, dtype=np.float64)
+    lq, G, d = qg.shape
+    lk = kg.shape[0]
+    out = np.zeros((lq, G, d))
+    lse = np.zeros((lq, G))
+    dq = np.zeros((lq, G, d))
+    dk = np.zeros((lk, d))
+    dv = np.zeros((lk, d))
+    if lq == 0:
+        return out, lse, dq, dk, dv
+    if lk == 0:
+        lse[:] = -np.inf
+        return out, lse, dq, dk, dv
+    for j in range(G):
+        s = _scores(qg[:, j, :], kg, scale, causal)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        l = e.sum(axis=1)
+        p = e / l[:, None]
+        lse[:, j] = m + np.log(l)
+        out[:, j, :] = p @ vg
+        do = dog[:, j, :]
+        dv += p.T @ do
+        dp = do @ vg.T
+        dsum = (p * dp).sum(axis=1)
+        ds = p * (dp - dsum[:, None])
+        dq[:, j, :] = scale * (ds @ kg)
+        dk += scale * (ds.T @ qg[:, j, :])
+    return out, lse, dq, dk, dv
+
+
+def attn_group_bwd_given(qg, kg, vg, outg, dog, lseg, scale, causal):
+    """Backward for one sequence and key/value group from a supplied ``out``/``lse``.
+
+    This is the interface TransformerEngine's ``fused_attn_bwd`` exposes (issue
+    #2448 reproduction: ``q, k, v, out, dout`` plus the aux tensor ``lse``):
+    ``P = exp(S - lse)``, ``D = rowsum(dout * out)``, then the same products as
+    :func:`attn_group_fwd_bwd`. When ``out, lse`` are the exact forward results the
+    two functions agree (``sum_j P_ij dP_ij = dO_i . O_i``).
+    Parity: pinned against :func:`attn_group_fwd_bwd` and torch autograd.
+    """
+    qg = np.asarray(qg, dtype=np.float64)
+    kg = np.asarray(kg, dtype=np.float64)
+    vg = np.asarray(vg, dtype=np.float64)
+    outg = np.asarray(outg, dtype=np.float64)
+    dog = np.asarray(dog, dtype=np.float64)
+    lseg = np.asarray(lseg, dtype=np.float64)
+    lq, G, d = qg.shape
+    lk = kg.shape[0]
+    dq = np.zeros((lq, G, d))
+    dk = np.zeros((lk, d))
+    dv = np.zeros((lk, d))
+    if lq == 0 or lk == 0:
+        return dq, dk, dv
+    for j in range(G):
+        s = _scores(qg[:, j, :], kg, scale, causal)
+        p = np.exp(s - lseg[:, j][:, None])
+        do = dog[:, j, :]
+        dv += p.T @ do
+        dp = do @ vg.T
+        dsum = (do * outg[:, j, :]).sum(axis=1)
+        ds = p * (dp - dsum[:, None])
+        dq[:, j, :] = scale * (ds @ kg)
+        dk += scale * (ds.T @ qg[:, j, :])
+    return dq, dk, dv
+
+
+def _check_heads(q, k):
+    hq, hkv = q.shape[1], k.shape[1]
+    if hkv < 1 or hq % hkv != 0:
+        raise ValueError("hq must be a positive multiple of hkv")
+    return hq, hkv, hq // hkv
+
+
+def attn_fwd_bwd_thd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv,
+                     cu_seqlens_q_padded, cu_seqlens_kv_padded, attn_scale,
+                     mask_type):
+    """THD forward + backward: ``(out, lse, dq, dk, dv)`` in float64, padded layout.
+
+    Loops over sequences and key/value heads and calls :func:`attn_group_fwd_bwd`
+    on the real rows; every other row stays exactly 0 (issue #2448 "Expected
+    behavior"; issue #2892: output keeps the padded shape of Q).
+    Parity: pinned.
+    """
+    causal = _is_causal(mask_type)
+    hq, hkv, G = _check_heads(q, k)
+    qs = seq_spans(cu_seqlens_q, cu_seqlens_q_padded)
+    ks = seq_spans(cu_seqlens_kv, cu_seqlens_kv_padded)
+    if len(qs) != len(ks):
+        raise ValueError("q and kv cu_seqlens describe different batch sizes")
+    Tq, _, d = q.shape
+    Tk = k.shape[0]
+    out = np.zeros((Tq, hq, d))
+    lse = np.zeros((Tq, hq))
+    dq = np.zeros((Tq, hq, d))
+    dk = np.zeros((Tk, hkv, d))
+    dv = np.zeros((Tk, hkv, d))
+    for (oq, lq), (ok, lk) in zip(qs, ks):
+        if oq + lq > Tq or ok + lk > Tk:
+            raise ValueError("padded offsets run past the tensors")
+        for g in range(hkv):
+            hs = slice(g * G, (g + 1) * G)
+            o, l, a, b_, c = attn_group_fwd_bwd(
+                q[oq:oq + lq, hs], k[ok:ok + lk, g], v[ok:ok + lk, g],
+                dout[oq:oq + lq, hs], attn_scale, causal)
+            out[oq:oq + lq, hs] = o
+            lse[oq:oq + lq, hs] = l
+            dq[oq:oq + lq, hs] = a
+            dk[ok:ok + lk, g] = b_
+            dv[ok:ok + lk, g] = c
+    return out, lse, dq, dk, dv
+
+
+def attn_fwd_thd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                 cu_seqlens_kv_padded, attn_scale, mask_type):
+    """THD forward only: ``(out, lse)``. Same arithmetic as the forward half of
+    :func:`attn_fwd_bwd_thd` (called with a zero upstream gradient).
+    Parity: pinned."""
+    zero = np.zeros(q.shape)
+    out, lse, _, _, _ = attn_fwd_bwd_thd(
+        q, k, v, zero, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+        cu_seqlens_kv_padded, attn_scale, mask_type)
+    return out, lse
+
+
+def attn_bwd_thd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv,
+                 cu_seqlens_q_padded, cu_seqlens_kv_padded, attn_scale, mask_type):
+    """THD backward from supplied ``out`` and ``lse``: ``(dq, dk, dv)`` float64.
+
+    The interface of TransformerEngine's ``fused_attn_bwd`` (issue #2448
+    reproduction). Rows that are not real tokens, and key/value rows that no valid
+    query sees, are exactly 0.
+    Parity: pinned."""
+    causal = _is_causal(mask_type)
+    hq, hkv, G = _check_heads(q, k)
+    qs = seq_spans(cu_seqlens_q, cu_seqlens_q_padded)
+    ks = seq_spans(cu_seqlens_kv, cu_seqlens_kv_padded)
+    if len(qs) != len(ks):
+        raise ValueError("q and kv cu_seqlens describe different batch sizes")
+    Tq, _, d = q.shape
+    Tk = k.shape[0]
+    dq = np.zeros((Tq, hq, d))
+    dk = np.zeros((Tk, hkv, d))
+    dv = np.zeros((Tk, hkv, d))
+    for (oq, lq), (ok, lk) in zip(qs, ks):
+        for g in range(hkv):
+            hs = slice(g * G, (g + 1) * G)
+            a, b_, c = attn_group_bwd_given(
+                q[oq:oq + lq, hs], k[ok:ok + lk, g], v[ok:ok + lk, g],
+                out[oq:oq + lq, hs], dout[oq:oq + lq, hs], lse[oq:oq + lq, hs],
+                attn_scale, causal)
+            dq[oq:oq + lq, hs] = a
+            dk[ok:ok + lk, g] = b_
+            dv[ok:ok + lk, g] = c
+    return dq, dk, dv
+
+
+def valid_row_masks(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                    cu_seqlens_kv_padded, T_q, T_kv, mask_type):
+    """Which rows may be nonzero: ``(q_rows [T_q], kv_rows [T_kv])`` booleans.
+
+    A query row may be nonzero iff it is a real token of a sequence with at least
+    one real key; a key/value row may be nonzero in dk/dv iff it is a real token that
+    some real query sees (padding: the sequence has a query; padding_causal: also
+    its index is below the query length, since query i sees keys j <= i).
+    Every other row must be exactly 0 (issue #2448 "Expected behavior").
+    Parity: pinned by the golden fixtures of issues #2448 and #2892.
+    """
+    causal = _is_causal(mask_type)
+    qs = seq_spans(cu_seqlens_q, cu_seqlens_q_padded)
+    ks = seq_spans(cu_seqlens_kv, cu_seqlens_kv_padded)
+    qm = np.zeros(T_q, dtype=bool)
+    km = np.zeros(T_kv, dtype=bool)
+    for (oq, lq), (ok, lk) in zip(qs, ks):
+        if lk > 0:
+            qm[oq:oq + lq] = True
+        if lq > 0:
+            seen = min(lk, lq) if causal else lk
+            km[ok:ok + seen] = True
+    return qm, km
+
+
+def fwd_bwd_flops(cu_seqlens_q, cu_seqlens_kv, hq, d, mask_type):
+    """Causal-adjusted algorithmic FLOPs of forward + backward (test helper).
+
+    Per (sequence, query head): ``F_fwd = 4 d pairs`` with ``pairs = Lq Lk``
+    (padding) or ``Lq Lk / 2`` (padding_causal); forward + backward is ``3.5 F_fwd``
+    (2 GEMMs forward, 5 backward)."""
+    causal = _is_causal(mask_type)
+    lq = np.diff(np.asarray(cu_seqlens_q, dtype=np.int64)).astype(np.float64)
+    lk = np.diff(np.asarray(cu_seqlens_kv, dtype=np.int64)).astype(np.float64)
+    pairs = lq * lk * (0.5 if causal else 1.0)
+    return float(3.5 * 4.0 * d * hq * pairs.sum())
