@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) attention forward/backward over packed variable-length sequences.
+
+The compute lives in ``lib/libteattn.so`` (C ABI in ``include/te_attn.h``); this
+package marshals torch tensors into that ABI and nothing more. There is no CPU
+path: every function raises if the library is missing or a tensor is not on a
+CUDA device.
+"""
+
+from ._binding import (  # noqa: F401
+    MASK_PADDING,
+    MASK_PADDING_CAUSAL,
+    TeAttnError,
+    bwd,
+    fwd,
+    fwd_workspace_size,
+    bwd_workspace_size,
+    library,
+    library_path,
+    read_status,
+    version,
+)

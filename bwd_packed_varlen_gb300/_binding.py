@@ -1,0 +1,182 @@
+"""ctypes binding of libteattn.so: argument marshalling only.
+
+Names mirror the C ABI (``te_attn_fwd_thd`` -> :func:`fwd`, ``te_attn_bwd_thd`` ->
+:func:`bwd`). Tensors are passed by ``data_ptr()``; the current torch CUDA stream
+is passed as the launch stream; output and workspace buffers are allocated with
+torch when the caller does not supply them.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+MASK_PADDING = 1
+MASK_PADDING_CAUSAL = 2
+_MASK_NAMES = {"padding": MASK_PADDING, "padding_causal": MASK_PADDING_CAUSAL}
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libteattn.so")
+_lib = None
+
+
+class TeAttnError(RuntimeError):
+    """A libteattn call returned a nonzero status."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libteattn error {code}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load libteattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+            "g.build()'` (or python bwd_packed_varlen_gb300/build.py)")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.te_attn_version.restype = i32
+    L.te_attn_version.argtypes = []
+    for name in ("te_attn_fwd_workspace_size", "te_attn_bwd_workspace_size"):
+        fn = getattr(L, name)
+        fn.restype = sz
+        fn.argtypes = [i32] * 6
+    L.te_attn_fwd_thd.restype = i32
+    L.te_attn_fwd_thd.argtypes = [vp] * 5 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_bwd_thd.restype = i32
+    L.te_attn_bwd_thd.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_read_status.restype = i32
+    L.te_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
+    L.te_attn_last_error.restype = ctypes.c_char_p
+    L.te_attn_last_error.argtypes = []
+    _lib = L
+    return L
+
+
+def version() -> int:
+    return int(library().te_attn_version())
+
+
+def _mask(mask_type) -> int:
+    if isinstance(mask_type, str):
+        if mask_type not in _MASK_NAMES:
+            raise ValueError(f"unknown mask_type {mask_type!r}")
+        return _MASK_NAMES[mask_type]
+    return int(mask_type)
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise TeAttnError(rc, library().te_attn_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _cu(*cus):
+    for c in cus:
+        if c.dtype != torch.int32:
+            raise ValueError("cu_seqlens tensors must be int32")
+
+
+def fwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
+    return int(library().te_attn_fwd_workspace_size(batch, total_q, total_kv, hq, hkv, d))
+
+
+def bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
+    return int(library().te_attn_bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d))
+
+
+def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+        attn_scale, mask_type="padding", max_seqlen_q=0, max_seqlen_kv=0, out=None, lse=None,
+        workspace=None, stream=None):
+    """``te_attn_fwd_thd``: returns ``(out, lse)``; out ``[T_q, hq, d]`` in q's dtype,
+    lse ``[T_q, hq]`` fp32."""
+    L = library()
+    _need_cuda(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+               cu_seqlens_kv_padded, out, lse, workspace)
+    _cu(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    Tq, hq, d = q.shape
+    Tk, hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Tq, hq), dtype=torch.float32, device=q.device)
+    need = fwd_workspace_size(B, Tq, Tk, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    rc = L.te_attn_fwd_thd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk,
+        int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, d, float(attn_scale), _mask(mask_type),
+        _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st))
+    _check(rc)
+    return out, lse
+
+
+def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+        cu_seqlens_kv_padded, attn_scale, mask_type="padding", max_seqlen_q=0,
+        max_seqlen_kv=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """``te_attn_bwd_thd``: returns ``(dq, dk, dv)`` in q's dtype."""
+    L = library()
+    _need_cuda(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+               cu_seqlens_kv_padded, dq, dk, dv, workspace)
+    _cu(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded)
+    if q.dtype not in _DTYPES or any(t.dtype != q.dtype for t in (k, v, out, dout)):
+        raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    Tq, hq, d = q.shape
+    Tk, hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_size(B, Tq, Tk, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    rc = L.te_attn_bwd_thd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
+        _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+        d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace),
+        workspace.numel(), ctypes.c_void_p(st))
+    _check(rc)
+    return dq, dk, dv
+
+
+def read_status(workspace, stream=None) -> int:
+    """Synchronise and return the device status word of the last call that used
+    ``workspace`` (0 clean; bit 1 inconsistent cu_seqlens; bit 2 wait timeout)."""
+    L = library()
+    st = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
+    val = ctypes.c_int(0)
+    _check(L.te_attn_read_status(_ptr(workspace), ctypes.byref(val), ctypes.c_void_p(st)))
+    return int(val.value)

@@ -1,0 +1,623 @@
+// Backward attention over packed variable-length sequences on sm_103a.
+//
+// Two tensor-core kernels, both with the role split of the forward kernel
+// (warp 4 TMA, warp 5 one MMA-issuing thread, warps 0-3 one thread per TMEM lane):
+//
+// dK/dV kernel -- item = (sequence b, key/value head g, 128-row key tile).
+//   K and V of the tile stay in shared memory for the whole item; the item sweeps
+//   the G query heads of the group and, for each, the query tiles that can see
+//   the key tile (causal: from the diagonal on), in a fixed order:
+//     S^T  = K Q^T,  dP^T = V dO^T                      (tcgen05, into TMEM)
+//     P^T  = exp(S^T - lse), dS^T = P^T (dP^T - D)      (one thread per key row;
+//            masked entries are selected to exact 0, so pad-slot values never
+//            leak; P^T and dS^T are written back over S^T / dP^T as 16-bit)
+//     dV  += P^T dO,  dK += dS^T Q                      (A operands from TMEM)
+//   dK/dV accumulate in TMEM over the whole group, so the GQA reduction happens
+//   inside one block with no atomics: results are deterministic.
+//   For head_dim > 128 the tile sweeps 64 query rows per step and each block
+//   produces half of the output columns (two blocks per item).
+//
+// dQ kernel -- item = (sequence b, query head h, 128-row query tile); Q and dO stay
+//   in shared memory, key tiles stream: S = Q K^T, dP = dO V^T, dS = P (dP - D),
+//   dQ += dS K with dQ in TMEM.
+//
+// Both scale by attn_scale in the epilogue and store only rows that belong to
+// real tokens (and, for dK/dV, that some real query sees); every other row is
+// written as exact zero by the zero-fill kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "sm103_ptx.cuh"
+#include "tmap.h"
+
+namespace teattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2b(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool kBF16>
+using elem_t = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+
+// Store 32 fp32 values (scaled) as 16-bit to row[c0 .. c0+32), columns < d only.
+template <bool kBF16>
+__device__ __forceinline__ void store_row32(elem_t<kBF16>* row, int c0, int d, const uint32_t (&v)[32],
+                                            float scale) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int col = c0 + q * 8;
+    if (col + 8 <= d) {
+      uint4 w;
+      w.x = pack2<kBF16>(__uint_as_float(v[q * 8 + 0]) * scale, __uint_as_float(v[q * 8 + 1]) * scale);
+      w.y = pack2<kBF16>(__uint_as_float(v[q * 8 + 2]) * scale, __uint_as_float(v[q * 8 + 3]) * scale);
+      w.z = pack2<kBF16>(__uint_as_float(v[q * 8 + 4]) * scale, __uint_as_float(v[q * 8 + 5]) * scale);
+      w.w = pack2<kBF16>(__uint_as_float(v[q * 8 + 6]) * scale, __uint_as_float(v[q * 8 + 7]) * scale);
+      *reinterpret_cast<uint4*>(row + col) = w;
+    }
+  }
+}
+
+// ===========================================================================
+// dK / dV
+// ===========================================================================
+template <int kD>
+struct DkdvShape {
+  static constexpr int kBM = kD <= 128 ? 128 : 64;   // query rows per step
+  static constexpr int kSplit = kD <= 128 ? 1 : 2;   // output column halves
+  static constexpr int kDo = kD / kSplit;            // output columns per block
+  static constexpr int kChunks = kD / 64;
+  static constexpr int kKVBytes = kChunks * 16384;   // one 128-row K or V tile
+  static constexpr int kQBytes = kChunks * kBM * 128; // one kBM-row Q or dO tile
+  static constexpr int kStages = (2 * kKVBytes + 4 * kQBytes + 4 * kBM * 4 + 2048 <= 227 * 1024) ? 2 : 1;
+  static constexpr int kSmemUsed = 2 * kKVBytes + kStages * 2 * kQBytes + kStages * 2 * kBM * 4 + 1024;
+  // At least 120 KB so that one block owns an SM (and all of TMEM).
+  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr uint32_t kColDK = 0, kColDV = 128, kColST = 256, kColDPT = 256 + kBM;
+};
+
+template <int kD, bool kBF16>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV) {
+  using S = DkdvShape<kD>;
+  constexpr int kBM = S::kBM, NS = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + S::kKVBytes;
+  uint8_t* sQ = sV + S::kKVBytes;             // NS stages
+  uint8_t* sDO = sQ + NS * S::kQBytes;        // NS stages
+  float* sLse = reinterpret_cast<float*>(sDO + NS * S::kQBytes);  // NS x kBM (log2 domain)
+  float* sDelta = sLse + NS * kBM;                                 // NS x kBM
+
+  __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_acc_full, bar_acc_empty;
+  __shared__ uint64_t bar_q_full[NS], bar_q_empty[NS];
+  __shared__ uint64_t bar_s_full, bar_ds_ready;
+  __shared__ uint32_t tmem_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* status = p.header + kHdrStatus;
+  const int per_pair = p.hkv * S::kSplit;
+  const int n_items = p.header[kHdrNumKPairs] * per_pair;
+  const bool causal = p.causal != 0;
+
+  if (tid == 0) {
+    mbar_init(&bar_kv_full, 1);
+    mbar_init(&bar_kv_empty, 1);
+    mbar_init(&bar_acc_full, 1);
+    mbar_init(&bar_acc_empty, 128);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bar_q_full[i], 1 + 32);
+      mbar_init(&bar_q_empty[i], 1);
+    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_ds_ready, 128);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // Per-item geometry, identical in every role.
+  struct Item {
+    SeqInfo s;
+    int kt, g, split, qt0, nq, steps;
+  };
+  auto decode = [&](int item) {
+    Item it;
+    const int2 pr = p.k_pairs[item / per_pair];
+    const int rem = item % per_pair;
+    it.g = rem / S::kSplit;
+    it.split = rem % S::kSplit;
+    it.kt = pr.y;
+    it.s = load_seq(p, pr.x);
+    it.qt0 = causal ? (it.kt * kBlockN) / kBM : 0;
+    it.nq = (it.s.len_q + kBM - 1) / kBM;
+    it.steps = p.group * (it.nq - it.qt0);
+    return it;
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- producer
+    int it = 0, ii = 0;
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmDO);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      const Item I = decode(item);
+      if (ii > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv_empty, (ii - 1) & 1, status));
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_kv_full, 2 * S::kKVBytes);
+        for (int c = 0; c < S::kChunks; ++c) {
+          tma_load_3d(sK + c * 16384, &tmK, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
+          tma_load_3d(sV + c * 16384, &tmV, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
+        }
+      }
+      const int nqt = I.nq - I.qt0;
+      for (int t = 0; t < I.steps; ++t, ++it) {
+        const int h = I.g * p.group + t / nqt;
+        const int qt = I.qt0 + t % nqt;
+        const int st = it % NS;
+        if (it >= NS) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_empty[st], ((it / NS) - 1) & 1, status));
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_q_full[st], 2 * S::kQBytes);
+          for (int c = 0; c < S::kChunks; ++c) {
+            tma_load_3d(sQ + st * S::kQBytes + c * kBM * 128, &tmQ, &bar_q_full[st], c * 64, h,
+                        I.s.off_q + qt * kBM);
+            tma_load_3d(sDO + st * S::kQBytes + c * kBM * 128, &tmDO, &bar_q_full[st], c * 64, h,
+                        I.s.off_q + qt * kBM);
+          }
+        }
+        for (int r = lane; r < kBM; r += 32) {
+          const int row = qt * kBM + r;
+          const bool valid = row < I.s.len_q;
+          const size_t gi = static_cast<size_t>(I.s.off_q + row) * p.hq + h;
+          sLse[st * kBM + r] = valid ? p.lse_in[gi] * kLog2e : 0.f;
+          sDelta[st * kBM + r] = valid ? p.delta[gi] : 0.f;
+        }
+        mbar_arrive(&bar_q_full[st]);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
+      constexpr uint32_t idAcc = make_idesc_f16(kBF16, false, true, 128, S::kDo);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+      const uint32_t t_dk = tmem + S::kColDK, t_dv = tmem + S::kColDV;
+      const uint32_t t_st = tmem + S::kColST, t_dpt = tmem + S::kColDPT;
+      int it = 0, ii = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+        const Item I = decode(item);
+        if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
+        const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
+        for (int t = 0; t < I.steps; ++t, ++it) {
+          const int st = it % NS;
+          if (!(ok = mbar_wait(&bar_q_full[st], (it / NS) & 1, status))) break;
+          tc_fence_after();
+          const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
+#pragma unroll
+          for (int s = 0; s < kD / 16; ++s) {
+            const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
+            const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
+            mma_ss(t_st, make_smem_desc(k_addr + ok_off, 16, 1024, kLayoutSW128),
+                   make_smem_desc(qb + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int s = 0; s < kD / 16; ++s) {
+            const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
+            const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
+            mma_ss(t_dpt, make_smem_desc(v_addr + ok_off, 16, 1024, kLayoutSW128),
+                   make_smem_desc(dob + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_s_full);
+          if (!(ok = mbar_wait(&bar_ds_ready, it & 1, status))) break;
+          if (t == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < kBM / 16; ++s) {
+            const uint32_t acc = (t > 0 || s > 0) ? 1u : 0u;
+            mma_ts(t_dv, t_st + s * 8,
+                   make_smem_desc(dob + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
+            mma_ts(t_dk, t_dpt + s * 8,
+                   make_smem_desc(qb + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
+          }
+          mma_commit(&bar_q_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar_kv_empty);
+        mma_commit(&bar_acc_full);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- compute
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_st = tmem + S::kColST + lane_base, t_dpt = tmem + S::kColDPT + lane_base;
+    const float sl2 = p.scale_log2;
+    int it = 0, ii = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      const Item I = decode(item);
+      const int kv_row = I.kt * kBlockN + tid;
+      const bool kv_valid = kv_row < I.s.len_k;
+      const int nqt = I.nq - I.qt0;
+      for (int t = 0; t < I.steps; ++t, ++it) {
+        const int qt = I.qt0 + t % nqt;
+        const int st = it % NS;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_full[st], (it / NS) & 1, status));
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        const float* lse2 = sLse + st * kBM;
+        const float* dlt = sDelta + st * kBM;
+        // query columns i with a nonzero P^T for this key row: [lo, hi)
+        const int q_base = qt * kBM;
+        const int hi = kv_valid ? min(kBM, I.s.len_q - q_base) : 0;
+        const int lo = causal ? max(0, kv_row - q_base) : 0;
+#pragma unroll
+        for (int c = 0; c < kBM / 32; ++c) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(t_st + c * 32, sv);
+          tmem_ld32(t_dpt + c * 32, dv);
+          tmem_ld_wait();
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i0 = c * 32 + 2 * k, i1 = i0 + 1;
+            const bool m0 = i0 >= lo && i0 < hi, m1 = i1 >= lo && i1 < hi;
+            const float p0 = m0 ? ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2[i0])) : 0.f;
+            const float p1 = m1 ? ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2[i1])) : 0.f;
+            const float d0 = m0 ? p0 * (__uint_as_float(dv[2 * k]) - dlt[i0]) : 0.f;
+            const float d1 = m1 ? p1 * (__uint_as_float(dv[2 * k + 1]) - dlt[i1]) : 0.f;
+            pp[k] = pack2<kBF16>(p0, p1);
+            dd[k] = pack2<kBF16>(d0, d1);
+          }
+          tmem_st16(t_st + c * 16, pp);
+          tmem_st16(t_dpt + c * 16, dd);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_ds_ready);
+      }
+      if (!ok) break;
+      // Epilogue: scale * dK and dV for rows some real query sees.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      const bool store = kv_row < seen_keys(I.s, causal);
+      elem_t<kBF16>* dk_row = static_cast<elem_t<kBF16>*>(p.dk) +
+                              (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
+      elem_t<kBF16>* dv_row = static_cast<elem_t<kBF16>*>(p.dv) +
+                              (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
+      const int col0 = I.split * S::kDo;
+#pragma unroll
+      for (int c0 = 0; c0 < S::kDo; c0 += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + S::kColDK + lane_base + c0, a);
+        tmem_ld32(tmem + S::kColDV + lane_base + c0, b);
+        tmem_ld_wait();
+        if (store) {
+          store_row32<kBF16>(dk_row, col0 + c0, p.d, a, p.scale);
+          store_row32<kBF16>(dv_row, col0 + c0, p.d, b, 1.0f);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+template <int kD>
+struct DqShape {
+  static constexpr int kBN = kD <= 128 ? 128 : 64;   // key rows per step
+  static constexpr int kChunks = kD / 64;
+  static constexpr int kQBytes = kChunks * 16384;    // 128-row Q or dO tile
+  static constexpr int kKVBytes = kChunks * kBN * 128;
+  static constexpr int kStages = (2 * kQBytes + 4 * kKVBytes + 2048 <= 227 * 1024) ? 2 : 1;
+  static constexpr int kSmemUsed = 2 * kQBytes + kStages * 2 * kKVBytes + 1024;
+  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr uint32_t kColDQ = 0, kColS = kD, kColDP = kD + kBN;
+};
+
+template <int kD, bool kBF16>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV) {
+  using S = DqShape<kD>;
+  constexpr int kBN = S::kBN, NS = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = sQ + S::kQBytes;
+  uint8_t* sK = sDO + S::kQBytes;          // NS stages
+  uint8_t* sV = sK + NS * S::kKVBytes;     // NS stages
+
+  __shared__ uint64_t bar_q_full, bar_q_empty, bar_acc_full, bar_acc_empty;
+  __shared__ uint64_t bar_kv_full[NS], bar_kv_empty[NS];
+  __shared__ uint64_t bar_s_full, bar_ds_ready;
+  __shared__ uint32_t tmem_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* status = p.header + kHdrStatus;
+  const int n_items = p.header[kHdrNumQPairs] * p.hq;
+  const bool causal = p.causal != 0;
+
+  if (tid == 0) {
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
+    mbar_init(&bar_acc_full, 1);
+    mbar_init(&bar_acc_empty, 128);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bar_kv_full[i], 1);
+      mbar_init(&bar_kv_empty[i], 1);
+    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_ds_ready, 128);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmDO);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int it = 0, ii = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+        const int2 pr = p.q_pairs[item / p.hq];
+        const int h = item % p.hq, g = h / p.group;
+        const SeqInfo s = load_seq(p, pr.x);
+        const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+        if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
+        mbar_arrive_expect_tx(&bar_q_full, 2 * S::kQBytes);
+        for (int c = 0; c < S::kChunks; ++c) {
+          tma_load_3d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.off_q + pr.y * kBlockM);
+          tma_load_3d(sDO + c * 16384, &tmDO, &bar_q_full, c * 64, h, s.off_q + pr.y * kBlockM);
+        }
+        for (int j = 0; j < n; ++j, ++it) {
+          const int st = it % NS;
+          if (it >= NS && !(ok = mbar_wait(&bar_kv_empty[st], ((it / NS) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bar_kv_full[st], 2 * S::kKVBytes);
+          for (int c = 0; c < S::kChunks; ++c) {
+            tma_load_3d(sK + st * S::kKVBytes + c * kBN * 128, &tmK, &bar_kv_full[st], c * 64, g,
+                        s.off_k + j * kBN);
+            tma_load_3d(sV + st * S::kKVBytes + c * kBN * 128, &tmV, &bar_kv_full[st], c * 64, g,
+                        s.off_k + j * kBN);
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
+      constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const uint32_t t_dq = tmem + S::kColDQ, t_s = tmem + S::kColS, t_dp = tmem + S::kColDP;
+      int it = 0, ii = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+        const int2 pr = p.q_pairs[item / p.hq];
+        const SeqInfo s = load_seq(p, pr.x);
+        const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+        if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
+        for (int j = 0; j < n; ++j, ++it) {
+          const int st = it % NS;
+          if (!(ok = mbar_wait(&bar_kv_full[st], (it / NS) & 1, status))) break;
+          tc_fence_after();
+          const uint32_t kb = k_addr + st * S::kKVBytes, vb = v_addr + st * S::kKVBytes;
+#pragma unroll
+          for (int s2 = 0; s2 < kD / 16; ++s2) {
+            const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+            const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
+            mma_ss(t_s, make_smem_desc(q_addr + oq, 16, 1024, kLayoutSW128),
+                   make_smem_desc(kb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int s2 = 0; s2 < kD / 16; ++s2) {
+            const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+            const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
+            mma_ss(t_dp, make_smem_desc(do_addr + oq, 16, 1024, kLayoutSW128),
+                   make_smem_desc(vb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_s_full);
+          if (!(ok = mbar_wait(&bar_ds_ready, it & 1, status))) break;
+          if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int s2 = 0; s2 < kBN / 16; ++s2) {
+            mma_ts(t_dq, t_s + s2 * 8, make_smem_desc(kb + s2 * 2048, kBN * 128, 1024, kLayoutSW128),
+                   idDQ, (j > 0 || s2 > 0) ? 1u : 0u);
+          }
+          mma_commit(&bar_kv_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar_q_empty);
+        mma_commit(&bar_acc_full);
+      }
+    }
+  } else {
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + S::kColS + lane_base, t_dp = tmem + S::kColDP + lane_base;
+    const float sl2 = p.scale_log2;
+    int it = 0, ii = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      const int2 pr = p.q_pairs[item / p.hq];
+      const int h = item % p.hq;
+      const SeqInfo s = load_seq(p, pr.x);
+      const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+      const int row = pr.y * kBlockM + tid;
+      const bool row_valid = row < s.len_q;
+      const size_t gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
+      const float lse2 = row_valid ? p.lse_in[gi] * kLog2e : 0.f;
+      const float dlt = row_valid ? p.delta[gi] : 0.f;
+      const int lim = row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
+      for (int j = 0; j < n; ++j, ++it) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        const int nvalid = lim - j * kBN;
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(t_s + c * 32, sv);
+          tmem_ld32(t_dp + c * 32, dv);
+          tmem_ld_wait();
+          uint32_t dd[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i0 = c * 32 + 2 * k, i1 = i0 + 1;
+            const float p0 = i0 < nvalid ? ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2)) : 0.f;
+            const float p1 = i1 < nvalid ? ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2)) : 0.f;
+            const float d0 = i0 < nvalid ? p0 * (__uint_as_float(dv[2 * k]) - dlt) : 0.f;
+            const float d1 = i1 < nvalid ? p1 * (__uint_as_float(dv[2 * k + 1]) - dlt) : 0.f;
+            dd[k] = pack2<kBF16>(d0, d1);
+          }
+          tmem_st16(t_s + c * 16, dd);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_ds_ready);
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
+      if (!ok) break;
+      tc_fence_after();
+      elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + gi * p.d;
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tmem + S::kColDQ + lane_base + c0, a);
+        tmem_ld_wait();
+        if (row_valid) store_row32<kBF16>(dq_row, c0, p.d, a, p.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// Launchers
+// ===========================================================================
+template <int kD, bool kBF16>
+static cudaError_t launch_dkdv_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
+  using S = DkdvShape<kD>;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16, S::kBM) ||
+      !make_tmap_thd(&tdo, p.dout, p.total_q, p.hq, p.d, kBF16, S::kBM) ||
+      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16, 128) ||
+      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16, 128))
+    return cudaErrorInvalidValue;
+  auto kern = attn_bwd_dkdv_kernel<kD, kBF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long max_items = static_cast<long long>(p.pair_cap_k) * p.hkv * S::kSplit;
+  const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
+  kern<<<grid, 192, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
+  return cudaGetLastError();
+}
+
+template <int kD, bool kBF16>
+static cudaError_t launch_dq_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
+  using S = DqShape<kD>;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16, 128) ||
+      !make_tmap_thd(&tdo, p.dout, p.total_q, p.hq, p.d, kBF16, 128) ||
+      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16, S::kBN) ||
+      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16, S::kBN))
+    return cudaErrorInvalidValue;
+  auto kern = attn_bwd_dq_kernel<kD, kBF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long max_items = static_cast<long long>(p.pair_cap_q) * p.hq;
+  const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
+  kern<<<grid, 192, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_dkdv(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st) {
+  const int d = p.d;
+  if (bf16) {
+    if (d <= 64) return launch_dkdv_impl<64, true>(p, num_sms, st);
+    if (d <= 128) return launch_dkdv_impl<128, true>(p, num_sms, st);
+    return launch_dkdv_impl<256, true>(p, num_sms, st);
+  }
+  if (d <= 64) return launch_dkdv_impl<64, false>(p, num_sms, st);
+  if (d <= 128) return launch_dkdv_impl<128, false>(p, num_sms, st);
+  return launch_dkdv_impl<256, false>(p, num_sms, st);
+}
+
+cudaError_t launch_attn_bwd_dq(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st) {
+  const int d = p.d;
+  if (bf16) {
+    if (d <= 64) return launch_dq_impl<64, true>(p, num_sms, st);
+    if (d <= 128) return launch_dq_impl<128, true>(p, num_sms, st);
+    return launch_dq_impl<256, true>(p, num_sms, st);
+  }
+  if (d <= 64) return launch_dq_impl<64, false>(p, num_sms, st);
+  if (d <= 128) return launch_dq_impl<128, false>(p, num_sms, st);
+  return launch_dq_impl<256, false>(p, num_sms, st);
+}
+
+}  // namespace teattn

@@ -1,0 +1,104 @@
+// Shared definitions of the attention kernels: launch parameters, workspace
+// header layout, tile sizes and the work-list decoding used by every kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace teattn {
+
+// Tile shape of the tensor-core kernels: 128 query rows (the M of one tcgen05
+// MMA) by 128 key rows per step.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+
+// Workspace header (int32 words at the start of every workspace).
+enum HeaderWord : int {
+  kHdrStatus = 0,    // TE_STATUS_* bits raised by this call's kernels
+  kHdrNumQPairs = 1, // number of (sequence, query tile) pairs
+  kHdrNumKPairs = 2, // number of (sequence, key tile) pairs
+  kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
+};
+
+constexpr int kStatusBadSeqlens = 1;
+constexpr int kStatusTimeout = 2;
+
+// Everything a kernel of this library needs, by value.
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out_in;  // backward: forward output (input)
+  const void* dout;
+  const float* lse_in; // backward: forward lse (input)
+  void* out;           // forward output
+  float* lse;          // forward lse output
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;        // backward: rowsum(dO * O), [total_q, hq]
+
+  const int* cu_q;
+  const int* cu_kv;
+  const int* cu_q_pad;
+  const int* cu_kv_pad;
+
+  int batch;
+  int total_q;
+  int total_kv;
+  int hq;
+  int hkv;
+  int d;
+  int group;         // hq / hkv
+  int causal;        // 1 for padding_causal
+  float scale;       // attn_scale
+  float scale_log2;  // attn_scale * log2(e)
+
+  int* header;       // workspace header (status, pair counts)
+  int2* q_pairs;     // sorted (sequence, query tile) pairs
+  int2* k_pairs;     // sorted (sequence, key tile) pairs
+  int pair_cap_q;    // capacity of q_pairs
+  int pair_cap_k;    // capacity of k_pairs
+};
+
+// Real length and padded offset of sequence b, validated against the tensor
+// extents. Returns false (length 0) for a sequence whose cu_seqlens are
+// inconsistent; the scheduler flags those in the status word.
+struct SeqInfo {
+  int off_q, len_q, off_k, len_k;
+  bool ok;
+};
+
+__device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
+  SeqInfo s;
+  int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+  int k0 = p.cu_kv[b], k1 = p.cu_kv[b + 1];
+  int pq0 = p.cu_q_pad[b], pq1 = p.cu_q_pad[b + 1];
+  int pk0 = p.cu_kv_pad[b], pk1 = p.cu_kv_pad[b + 1];
+  s.len_q = q1 - q0;
+  s.len_k = k1 - k0;
+  s.off_q = pq0;
+  s.off_k = pk0;
+  s.ok = s.len_q >= 0 && s.len_k >= 0 && pq0 >= 0 && pk0 >= 0 && s.len_q <= pq1 - pq0 &&
+         s.len_k <= pk1 - pk0 && pq1 <= p.total_q && pk1 <= p.total_kv;
+  if (!s.ok) {
+    s.len_q = 0;
+    s.len_k = 0;
+  }
+  return s;
+}
+
+// Number of key rows a query tile can see (upper-left causal: key j <= query i).
+__device__ __forceinline__ int visible_keys(const SeqInfo& s, int q_tile, bool causal) {
+  if (!causal) return s.len_k;
+  int last_q = min((q_tile + 1) * kBlockM, s.len_q);  // exclusive
+  return min(s.len_k, last_q);
+}
+
+// Number of key rows some real query sees (the rest get exact-zero dk/dv).
+__device__ __forceinline__ int seen_keys(const SeqInfo& s, bool causal) {
+  if (s.len_q == 0) return 0;
+  return causal ? min(s.len_k, s.len_q) : s.len_k;
+}
+
+}  // namespace teattn

@@ -1,0 +1,19 @@
+// Host-side launchers of the library's kernels (internal; the public surface is
+// include/te_attn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace teattn {
+
+cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, cudaStream_t st);
+cudaError_t launch_zero_fill(const AttnParams& p, int mode, int num_sms, cudaStream_t st);
+cudaError_t launch_delta(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+
+cudaError_t launch_attn_fwd(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_attn_bwd_dkdv(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_attn_bwd_dq(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+
+}  // namespace teattn

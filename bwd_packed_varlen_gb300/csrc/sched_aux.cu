@@ -1,0 +1,315 @@
+// Work scheduling (tile lists), exact-zero fill of rows no tile covers, and the
+// backward preprocess D = rowsum(dO * O). All three are memory- or latency-bound
+// SIMT kernels; the tensor-core kernels consume what they produce.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace teattn {
+
+// ---------------------------------------------------------------------------
+// Scheduler
+// ---------------------------------------------------------------------------
+// One 1024-thread block turns the four cu_seqlens arrays into two lists:
+//   q pairs  (sequence, query tile)  -- forward and dQ items (x hq heads)
+//   k pairs  (sequence, key tile)    -- dK/dV items (x hkv heads)
+// Tiles cover the REAL length of each sequence; sequences without a real query
+// or key produce no pair, and key tiles no real query sees (causal, beyond the
+// query length) produce none either -- those rows are zero-filled instead.
+// Each list is sorted by estimated cost (key tiles the item visits), largest
+// first, ties by natural order, so a persistent grid takes the long items first.
+// Up to kSortCap pairs are sorted in shared memory; a longer list keeps its
+// natural order. The result depends only on the cu_seqlens values.
+constexpr int kSchedThreads = 1024;
+constexpr int kSortCap = 8192;
+
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+// Last b in [0, B) with pref[b] <= i (pref is non-decreasing, pref[B] > i).
+__device__ __forceinline__ int find_seq(const int* pref, int B, int i) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ int q_pair_cost(const AttnParams& p, int b, int t) {
+  SeqInfo s = load_seq(p, b);
+  return (visible_keys(s, t, p.causal) + kBlockN - 1) / kBlockN;
+}
+
+__device__ int k_pair_cost(const AttnParams& p, int b, int t) {
+  SeqInfo s = load_seq(p, b);
+  int nq = (s.len_q + kBlockM - 1) / kBlockM;
+  return p.causal ? nq - (t * kBlockN) / kBlockM : nq;
+}
+
+template <bool kIsQ>
+__device__ void build_list(const AttnParams& p, const int* pref, int n, int2* out,
+                           uint64_t* keys) {
+  const int B = p.batch;
+  if (n <= kSortCap) {
+    int m = 1;
+    while (m < n) m <<= 1;
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      uint64_t key = ~0ull;
+      if (i < n) {
+        int b = find_seq(pref, B, i);
+        int t = i - pref[b];
+        int cost = kIsQ ? q_pair_cost(p, b, t) : k_pair_cost(p, b, t);
+        key = (static_cast<uint64_t>(0x7fffffffu - static_cast<uint32_t>(cost)) << 32) |
+              static_cast<uint32_t>(i);
+      }
+      keys[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= m; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+          int ixj = i ^ j;
+          if (ixj > i) {
+            uint64_t a = keys[i], c = keys[ixj];
+            bool up = (i & k) == 0;
+            if ((a > c) == up) {
+              keys[i] = c;
+              keys[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      int src = static_cast<int>(keys[i] & 0xffffffffu);
+      int b = find_seq(pref, B, src);
+      out[i] = make_int2(b, src - pref[b]);
+    }
+    __syncthreads();
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      int b = find_seq(pref, B, i);
+      out[i] = make_int2(b, i - pref[b]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, int* pref_q,
+                                                                  int* pref_k) {
+  extern __shared__ uint64_t sort_keys[];
+  __shared__ int warp_sums[32];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  int carry_q = 0, carry_k = 0;
+  for (int base = 0; base < p.batch; base += blockDim.x) {
+    int b = base + threadIdx.x;
+    int cq = 0, ck = 0;
+    if (b < p.batch) {
+      SeqInfo s = load_seq(p, b);
+      if (!s.ok) bad = 1;
+      if (s.len_q > 0 && s.len_k > 0) {
+        cq = (s.len_q + kBlockM - 1) / kBlockM;
+        ck = (seen_keys(s, p.causal) + kBlockN - 1) / kBlockN;
+      }
+    }
+    int tq, tk;
+    int eq = block_excl_scan(cq, warp_sums, &tq);
+    int ek = block_excl_scan(ck, warp_sums, &tk);
+    if (b < p.batch) {
+      pref_q[b] = carry_q + eq;
+      pref_k[b] = carry_k + ek;
+    }
+    carry_q += tq;
+    carry_k += tk;
+  }
+  if (threadIdx.x == 0) {
+    pref_q[p.batch] = carry_q;
+    pref_k[p.batch] = carry_k;
+  }
+  __threadfence_block();
+  __syncthreads();
+  const int nq = min(carry_q, p.pair_cap_q);
+  const int nk = min(carry_k, p.pair_cap_k);
+  build_list<true>(p, pref_q, nq, p.q_pairs, sort_keys);
+  build_list<false>(p, pref_k, nk, p.k_pairs, sort_keys);
+  if (threadIdx.x == 0) {
+    int status = bad ? kStatusBadSeqlens : 0;
+    if (carry_q > p.pair_cap_q || carry_k > p.pair_cap_k) status |= kStatusBadSeqlens;
+    p.header[kHdrStatus] = status;
+    p.header[kHdrNumQPairs] = nq;
+    p.header[kHdrNumKPairs] = nk;
+  }
+}
+
+cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, cudaStream_t st) {
+  const size_t smem = kSortCap * sizeof(uint64_t);
+  cudaError_t e = cudaFuncSetAttribute(schedule_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  schedule_kernel<<<1, kSchedThreads, smem, st>>>(p, pref_q, pref_k);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Row classification shared by the zero fill and the preprocess
+// ---------------------------------------------------------------------------
+// Sequence b whose padded span holds row r, or -1 (before the first span, after
+// the last, or inconsistent offsets).
+__device__ __forceinline__ int seq_of_row(const int* cu_pad, int B, int r) {
+  if (r < cu_pad[0] || r >= cu_pad[B]) return -1;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cu_pad[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// 0: not computed; 1: computed by a tensor-core kernel; 2: real query without keys.
+__device__ __forceinline__ int q_row_kind(const AttnParams& p, int r) {
+  int b = seq_of_row(p.cu_q_pad, p.batch, r);
+  if (b < 0) return 0;
+  SeqInfo s = load_seq(p, b);
+  if (r - s.off_q >= s.len_q) return 0;
+  return s.len_k > 0 ? 1 : 2;
+}
+
+__device__ __forceinline__ bool k_row_computed(const AttnParams& p, int r) {
+  int b = seq_of_row(p.cu_kv_pad, p.batch, r);
+  if (b < 0) return false;
+  SeqInfo s = load_seq(p, b);
+  return r - s.off_k < seen_keys(s, p.causal);
+}
+
+// ---------------------------------------------------------------------------
+// Zero fill: one warp per row, 16-byte stores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void zero_row(void* base, int r, int row_bytes) {
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(base) +
+                                        static_cast<size_t>(r) * row_bytes);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x & 31; i < row_bytes / 16; i += 32) dst[i] = z;
+}
+
+// mode 0: forward (out, lse); mode 1: backward (dq, dk, dv)
+__global__ void __launch_bounds__(256) zero_fill_kernel(AttnParams p, int mode) {
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qbytes = p.hq * p.d * 2, kbytes = p.hkv * p.d * 2;
+  for (int r = gw; r < p.total_q; r += warps) {
+    int kind = q_row_kind(p, r);
+    if (kind == 1) continue;
+    if (mode == 0) {
+      zero_row(p.out, r, qbytes);
+      float v = kind == 2 ? -INFINITY : 0.0f;
+      for (int h = lane; h < p.hq; h += 32) p.lse[static_cast<size_t>(r) * p.hq + h] = v;
+    } else {
+      zero_row(p.dq, r, qbytes);
+    }
+  }
+  if (mode == 1) {
+    for (int r = gw; r < p.total_kv; r += warps) {
+      if (k_row_computed(p, r)) continue;
+      zero_row(p.dk, r, kbytes);
+      zero_row(p.dv, r, kbytes);
+    }
+  }
+}
+
+cudaError_t launch_zero_fill(const AttnParams& p, int mode, int num_sms, cudaStream_t st) {
+  zero_fill_kernel<<<num_sms * 4, 256, 0, st>>>(p, mode);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Preprocess: delta[r, h] = sum_c float(dO[r,h,c]) * float(O[r,h,c]) on computed
+// rows, 0 elsewhere. One warp per row; lanes read 16-byte chunks. When d/8
+// divides 32 the lanes of one head are contiguous and reduce by shuffles;
+// otherwise each lane owns whole heads. Both orders are fixed (deterministic).
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
+  const T* x = reinterpret_cast<const T*>(&a);
+  const T* y = reinterpret_cast<const T*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = fmaf(static_cast<float>(x[i]), static_cast<float>(y[i]), s);
+  return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cpr = p.d / 8;  // 16-byte chunks per head
+  const int chunks = p.hq * cpr;
+  for (int r = gw; r < p.total_q; r += warps) {
+    const size_t row = static_cast<size_t>(r);
+    float* drow = p.delta + row * p.hq;
+    if (q_row_kind(p, r) != 1) {
+      for (int h = lane; h < p.hq; h += 32) drow[h] = 0.f;
+      continue;
+    }
+    const uint4* o = reinterpret_cast<const uint4*>(static_cast<const T*>(p.out_in) +
+                                                    row * p.hq * p.d);
+    const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) +
+                                                    row * p.hq * p.d);
+    if (32 % cpr == 0) {
+      for (int c0 = 0; c0 < chunks; c0 += 32) {
+        int c = c0 + lane;
+        float s = c < chunks ? dot8<T>(o[c], g[c]) : 0.f;
+        for (int w = cpr >> 1; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+        if (c < chunks && (c % cpr) == 0) drow[c / cpr] = s;
+      }
+    } else {
+      for (int h = lane; h < p.hq; h += 32) {
+        float s = 0.f;
+        for (int c = 0; c < cpr; ++c) s += dot8<T>(o[h * cpr + c], g[h * cpr + c]);
+        drow[h] = s;
+      }
+    }
+  }
+}
+
+cudaError_t launch_delta(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st) {
+  if (bf16)
+    delta_kernel<__nv_bfloat16><<<num_sms * 8, 256, 0, st>>>(p);
+  else
+    delta_kernel<__half><<<num_sms * 8, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace teattn

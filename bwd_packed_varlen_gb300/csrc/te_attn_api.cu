@@ -1,0 +1,287 @@
+// C ABI of libteattn.so (declared in include/te_attn.h): argument checks,
+// workspace layout and the launch sequence of each call.
+//
+//   forward : schedule -> attention forward -> zero fill (out, lse)
+//   backward: schedule -> D = rowsum(dO * O) -> dK/dV -> dQ -> zero fill (dq, dk, dv)
+//
+// All launches go to the caller's stream; nothing is allocated and nothing is
+// kept between calls except per-device constants (SM count).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "../../include/te_attn.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int ok_status() {
+  g_last_error.clear();
+  return TE_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t header, pref_q, pref_k, q_pairs, k_pairs, delta, total;
+  int cap_q, cap_k;
+};
+
+// Workspace layout (256-byte aligned sections):
+//   header  int32[64]        status word and pair counts of this call
+//   pref_q  int32[batch+1]   prefix sums of query tiles per sequence
+//   pref_k  int32[batch+1]   prefix sums of key tiles per sequence
+//   q_pairs int2[cap_q]      sorted (sequence, query tile)
+//   k_pairs int2[cap_k]      sorted (sequence, key tile)
+//   delta   fp32[total_q*hq] backward only: rowsum(dO * O)
+bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L) {
+  if (batch < 1 || total_q < 0 || total_kv < 0 || hq < 1) return false;
+  // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
+  const long long cq = static_cast<long long>(total_q) / teattn::kBlockM + batch + 1;
+  const long long ck = static_cast<long long>(total_kv) / teattn::kBlockN + batch + 1;
+  if (cq > INT32_MAX / 64 || ck > INT32_MAX / 64) return false;
+  L->cap_q = static_cast<int>(cq);
+  L->cap_k = static_cast<int>(ck);
+  size_t off = 0;
+  L->header = off;
+  off = align_up(off + teattn::kHdrWords * sizeof(int), 256);
+  L->pref_q = off;
+  off = align_up(off + (static_cast<size_t>(batch) + 1) * sizeof(int), 256);
+  L->pref_k = off;
+  off = align_up(off + (static_cast<size_t>(batch) + 1) * sizeof(int), 256);
+  L->q_pairs = off;
+  off = align_up(off + static_cast<size_t>(cq) * sizeof(int2), 256);
+  L->k_pairs = off;
+  off = align_up(off + static_cast<size_t>(ck) * sizeof(int2), 256);
+  L->delta = off;
+  if (backward) off = align_up(off + static_cast<size_t>(total_q) * hq * sizeof(float), 256);
+  L->total = off;
+  return true;
+}
+
+int num_sms_of_current_device() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared argument checks of both entry points. Returns TE_OK or an error code.
+int check_common(int batch, int total_q, int total_kv, int hq, int hkv, int d, float attn_scale,
+                 int mask_type, int dtype, const int32_t* cu_q, const int32_t* cu_kv,
+                 const int32_t* cu_q_pad, const int32_t* cu_kv_pad, const void* workspace) {
+  if (!cu_q || !cu_kv || !cu_q_pad || !cu_kv_pad)
+    return fail(TE_ERR_INVALID_ARG, "cu_seqlens pointers must not be NULL");
+  if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
+  if (batch < 1) return fail(TE_ERR_INVALID_ARG, "batch must be >= 1");
+  if (total_q < 0 || total_kv < 0) return fail(TE_ERR_INVALID_ARG, "total_q/total_kv must be >= 0");
+  if (hq < 1 || hkv < 1) return fail(TE_ERR_INVALID_ARG, "hq and hkv must be >= 1");
+  if (hq % hkv != 0) return fail(TE_ERR_INVALID_ARG, "hq must be a multiple of hkv");
+  if (d < 8 || d > 256 || d % 8 != 0)
+    return fail(TE_ERR_UNSUPPORTED, "head dim must be a multiple of 8 in [8, 256]");
+  if (mask_type != TE_MASK_PADDING && mask_type != TE_MASK_PADDING_CAUSAL)
+    return fail(TE_ERR_UNSUPPORTED, "mask_type must be TE_MASK_PADDING or TE_MASK_PADDING_CAUSAL");
+  if (dtype != TE_DTYPE_FP16 && dtype != TE_DTYPE_BF16)
+    return fail(TE_ERR_UNSUPPORTED, "dtype must be TE_DTYPE_FP16 or TE_DTYPE_BF16");
+  if (!std::isfinite(attn_scale)) return fail(TE_ERR_INVALID_ARG, "attn_scale must be finite");
+  if (static_cast<long long>(total_q) * hq * d >= (1ll << 40) ||
+      static_cast<long long>(total_kv) * hkv * d >= (1ll << 40))
+    return fail(TE_ERR_UNSUPPORTED, "tensor too large");
+  return TE_OK;
+}
+
+teattn::AttnParams base_params(const int32_t* cu_q, const int32_t* cu_kv, const int32_t* cu_q_pad,
+                               const int32_t* cu_kv_pad, int batch, int total_q, int total_kv, int hq,
+                               int hkv, int d, float attn_scale, int mask_type, void* workspace,
+                               const Layout& L) {
+  teattn::AttnParams p{};
+  p.cu_q = cu_q;
+  p.cu_kv = cu_kv;
+  p.cu_q_pad = cu_q_pad;
+  p.cu_kv_pad = cu_kv_pad;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.d = d;
+  p.group = hq / hkv;
+  p.causal = mask_type == TE_MASK_PADDING_CAUSAL ? 1 : 0;
+  p.scale = attn_scale;
+  p.scale_log2 = attn_scale * 1.4426950408889634f;
+  char* ws = static_cast<char*>(workspace);
+  p.header = reinterpret_cast<int*>(ws + L.header);
+  p.q_pairs = reinterpret_cast<int2*>(ws + L.q_pairs);
+  p.k_pairs = reinterpret_cast<int2*>(ws + L.k_pairs);
+  p.pair_cap_q = L.cap_q;
+  p.pair_cap_k = L.cap_k;
+  return p;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(TE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int te_attn_version(void) { return 10000; }
+
+size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
+  (void)hkv;
+  (void)d;
+  Layout L;
+  return make_layout(batch, total_q, total_kv, hq, false, &L) ? L.total : 0;
+}
+
+size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
+  (void)hkv;
+  (void)d;
+  Layout L;
+  return make_layout(batch, total_q, total_kv, hq, true, &L) ? L.total : 0;
+}
+
+int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, float* lse,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int batch,
+                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int hq, int hkv,
+                    int d, float attn_scale, int mask_type, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
+  int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
+                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                        workspace);
+  if (rc != TE_OK) return rc;
+  if (total_q > 0 && (!q || !out || !lse))
+    return fail(TE_ERR_INVALID_ARG, "q, out and lse must not be NULL");
+  if (total_kv > 0 && (!k || !v)) return fail(TE_ERR_INVALID_ARG, "k and v must not be NULL");
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (out && !aligned16(out)))
+    return fail(TE_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+  Layout L;
+  if (!make_layout(batch, total_q, total_kv, hq, false, &L))
+    return fail(TE_ERR_INVALID_ARG, "sizes out of range");
+  if (workspace_bytes < L.total)
+    return fail(TE_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than te_attn_fwd_workspace_size()");
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return fail(TE_ERR_CUDA, "no CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  teattn::AttnParams p = base_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                                     cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d,
+                                     attn_scale, mask_type, workspace, L);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  char* ws = static_cast<char*>(workspace);
+  int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
+  int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
+  const bool bf16 = dtype == TE_DTYPE_BF16;
+  cudaError_t e = teattn::launch_schedule(p, pref_q, pref_k, st);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  if (total_q > 0 && total_kv > 0) {
+    e = teattn::launch_attn_fwd(p, bf16, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attention forward");
+  }
+  if (total_q > 0) {
+    e = teattn::launch_zero_fill(p, 0, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+  }
+  return ok_status();
+}
+
+int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                    const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
+                    int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                    int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
+  int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
+                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                        workspace);
+  if (rc != TE_OK) return rc;
+  if (total_q > 0 && (!q || !out || !dout || !lse || !dq))
+    return fail(TE_ERR_INVALID_ARG, "q, out, dout, lse and dq must not be NULL");
+  if (total_kv > 0 && (!k || !v || !dk || !dv))
+    return fail(TE_ERR_INVALID_ARG, "k, v, dk and dv must not be NULL");
+  const void* ptrs[] = {q, k, v, out, dout, dq, dk, dv};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return fail(TE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  Layout L;
+  if (!make_layout(batch, total_q, total_kv, hq, true, &L))
+    return fail(TE_ERR_INVALID_ARG, "sizes out of range");
+  if (workspace_bytes < L.total)
+    return fail(TE_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than te_attn_bwd_workspace_size()");
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return fail(TE_ERR_CUDA, "no CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  teattn::AttnParams p = base_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                                     cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d,
+                                     attn_scale, mask_type, workspace, L);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out_in = out;
+  p.dout = dout;
+  p.lse_in = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  char* ws = static_cast<char*>(workspace);
+  p.delta = reinterpret_cast<float*>(ws + L.delta);
+  int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
+  int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
+  const bool bf16 = dtype == TE_DTYPE_BF16;
+  cudaError_t e = teattn::launch_schedule(p, pref_q, pref_k, st);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  if (total_q > 0) {
+    e = teattn::launch_delta(p, bf16, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "delta");
+  }
+  if (total_q > 0 && total_kv > 0) {
+    e = teattn::launch_attn_bwd_dkdv(p, bf16, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dK/dV");
+    e = teattn::launch_attn_bwd_dq(p, bf16, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dQ");
+  }
+  e = teattn::launch_zero_fill(p, 1, sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+  return ok_status();
+}
+
+int te_attn_read_status(const void* workspace, int* status, void* stream) {
+  if (!workspace || !status) return fail(TE_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  e = cudaMemcpy(status, static_cast<const char*>(workspace), sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status copy");
+  return ok_status();
+}
+
+const char* te_attn_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

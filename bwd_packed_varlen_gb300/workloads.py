@@ -136,26 +136,33 @@ def packings(lengths=(128,), seed: int = 42, H: int = 8, d: int = 128) -> Worklo
 
 
 def gqa_d256(seed: int = 3216, seq: int = 384, batch: int = 2, hq: int = 16,
-             hkv: int = 2, d: int = 256) -> Workload:
+             hkv: int = 2, d: int = 256, outlier: float = 20.0,
+             outlier_mode: str = "set") -> Workload:
     """Issue #3216 shape as THD: ``batch`` causal sequences of ``seq`` tokens,
     hq=16, hkv=2, d=256, scale 1/sqrt(d). q and k are N(0,1) times a per-channel
-    lognormal(0,1) scale (drawn separately for q and k), with the same 4 seeded
-    outlier channels multiplied by 20 in both, so q.k peaks and the softmax is
-    sharp; v and dout are N(0,1)."""
+    lognormal(0,1) scale (drawn separately for q and k); the same 4 seeded outlier
+    channels get scale ``outlier`` (20, i.e. 20x the median channel scale of 1) in
+    both, so q.k peaks and the softmax is sharp; v and dout are N(0,1).
+    ``outlier_mode="mul"`` multiplies the lognormal scale by ``outlier`` instead
+    (a harsher, heavier-tailed variant)."""
     rng = np.random.default_rng(seed)
     T = seq * batch
     sq = rng.lognormal(0.0, 1.0, size=d).astype(np.float32)
     sk = rng.lognormal(0.0, 1.0, size=d).astype(np.float32)
     outl = rng.choice(d, size=4, replace=False)
-    sq[outl] *= 20.0
-    sk[outl] *= 20.0
+    if outlier_mode == "mul":
+        sq[outl] *= outlier
+        sk[outl] *= outlier
+    else:
+        sq[outl] = outlier
+        sk[outl] = outlier
     q = _normal(rng, (T, hq, d)) * sq
     k = _normal(rng, (T, hkv, d)) * sk
     v = _normal(rng, (T, hkv, d))
     do = _normal(rng, (T, hq, d))
     cu = _cu([seq] * batch)
     return Workload(
-        name="gqa_d256", q=_to(q, "bf16"), k=_to(k, "bf16"), v=_to(v, "bf16"),
+        name=f"gqa_d256_{outlier_mode}", q=_to(q, "bf16"), k=_to(k, "bf16"), v=_to(v, "bf16"),
         dout=_to(do, "bf16"), cu_seqlens_q=cu.clone(), cu_seqlens_kv=cu.clone(),
         cu_seqlens_q_padded=cu.clone(), cu_seqlens_kv_padded=cu.clone(),
         attn_scale=1.0 / math.sqrt(d), mask_type=MASK_PADDING_CAUSAL, dtype="bf16",

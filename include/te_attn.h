@@ -1,0 +1,142 @@
+/*
+ * te_attn.h -- C ABI of libteattn.so: scaled-dot-product attention forward and
+ * backward over packed variable-length (THD) sequences, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (the TransformerEngine issues this library answers):
+ *   For each sequence b and query head h (key/value head g = h / (hq / hkv)):
+ *     S   = attn_scale * Q_b,h K_b,g^T        masked by the REAL lengths
+ *     P   = softmax(S) row-wise,  LSE = log(sum_j exp(S_ij))  (natural log)
+ *     O   = P V_b,g
+ *   and the gradient of sum(dO * O):
+ *     dV  = sum_{h in group} P^T dO,   dP = dO V^T,   D = rowsum(dO * O)
+ *     dS  = P * (dP - D),  dQ = attn_scale dS K,  dK = attn_scale sum_{h in group} dS^T Q
+ *   -- issue #2448 (THD + GQA fused_attn_bwd, "Expected behavior": rows of an empty
+ *      query sequence give exactly-zero dk/dv, results must not depend on earlier
+ *      calls), issue #3333 (THD padding_causal backward vs a per-sequence SDPA
+ *      reference), issue #3216 (GQA via repeat_interleave, causal = upper-left
+ *      triangle, head_dim 256 with batch >= 2), issue #2892 ("Expected Behavior":
+ *      cu_seqlens_* mask, cu_seqlens_*_padded index memory, output keeps the padded
+ *      layout).
+ *
+ * Layout (all tensors contiguous, row-major, device memory owned by the caller):
+ *   q, out, dout, dq : [total_q,  hq,  d]   16-bit (fp16 or bf16, all the same)
+ *   k, v, dk, dv     : [total_kv, hkv, d]   same dtype
+ *   lse              : [total_q,  hq]       fp32
+ *   cu_seqlens_q/kv          : int32 [batch+1] prefix sums of REAL lengths
+ *   cu_seqlens_q/kv_padded   : int32 [batch+1] prefix sums of PADDED lengths;
+ *       sequence b occupies rows cu_*_padded[b] .. cu_*_padded[b+1]-1 and its real
+ *       tokens are the first (cu_*[b+1]-cu_*[b]) of those rows.
+ *   Rows that are not real tokens (pad slots, tails after cu_*_padded[batch], rows
+ *   of empty sequences) are written as exact zeros in out/dq/dk/dv and 0 in lse;
+ *   key/value rows no real query sees are exact zeros in dk/dv. A real query of a
+ *   sequence with no real key gets out = 0, lse = -inf, dq = 0.
+ *   Pad slots may hold any finite values; they never reach a real output.
+ *
+ * Supported: d a multiple of 8 with 8 <= d <= 256; hq a positive multiple of hkv;
+ *   mask TE_MASK_PADDING or TE_MASK_PADDING_CAUSAL (key j visible to query i iff
+ *   j <= i, upper-left aligned); dtype TE_DTYPE_FP16 or TE_DTYPE_BF16.
+ *
+ * Determinism: no floating-point atomics; every output element is produced by one
+ *   thread block in a fixed order, so repeated calls on identical inputs give
+ *   bit-identical results regardless of call order, earlier calls, or the contents
+ *   of the output and workspace buffers on entry.
+ *
+ * Workspace: caller-allocated device memory of at least the size returned by the
+ *   matching *_workspace_size function. Its contents on entry are irrelevant: every
+ *   call rewrites what it reads. The library allocates no device memory and keeps no
+ *   state between calls. max_seqlen_q/kv are accepted for interface parity with
+ *   TransformerEngine and ignored (lengths come from the cu_seqlens arrays).
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *   default stream); no host synchronisation. Calls that share a workspace must be
+ *   ordered (same stream or explicit events).
+ *
+ * Errors: functions return TE_OK (0) or a negative TE_ERR_* code, and
+ *   te_attn_last_error() gives a thread-local message. Host-detectable argument
+ *   errors launch nothing. Errors that need device data (inconsistent cu_seqlens, a
+ *   pipeline wait that timed out) are recorded in a status word in the workspace;
+ *   te_attn_read_status() reads it after synchronising the stream.
+ */
+#ifndef TE_ATTN_H_
+#define TE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TE_MASK_PADDING 1
+#define TE_MASK_PADDING_CAUSAL 2
+
+#define TE_DTYPE_FP16 0
+#define TE_DTYPE_BF16 1
+
+#define TE_OK 0
+#define TE_ERR_INVALID_ARG (-1)
+#define TE_ERR_UNSUPPORTED (-2)
+#define TE_ERR_WORKSPACE_TOO_SMALL (-3)
+#define TE_ERR_CUDA (-4)
+#define TE_ERR_BAD_SEQLENS (-5)
+#define TE_ERR_TIMEOUT (-6)
+
+/* Device status bits reported by te_attn_read_status(). */
+#define TE_STATUS_BAD_SEQLENS 1
+#define TE_STATUS_TIMEOUT 2
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int te_attn_version(void);
+
+/* Bytes of workspace te_attn_fwd_thd needs for these sizes (0 on invalid sizes). */
+size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                  int d);
+
+/* Bytes of workspace te_attn_bwd_thd needs for these sizes (0 on invalid sizes). */
+size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                  int d);
+
+/*
+ * Forward: writes out [total_q, hq, d] and lse [total_q, hq] (natural-log softmax
+ * denominator of the scaled scores, fp32). Issue #2892 "Expected Behavior" fixes the
+ * real/padded split; issue #2448 passes lse to the backward as the aux tensor.
+ */
+int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, float* lse,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                    int batch, int total_q, int total_kv, int max_seqlen_q,
+                    int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                    int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Backward: from q, k, v, out, dout and lse, writes dq [total_q, hq, d],
+ * dk and dv [total_kv, hkv, d]. dk/dv of a key/value head sum over the hq/hkv query
+ * heads of its group inside one thread block (no atomics). The arguments mirror
+ * TransformerEngine's fused_attn_bwd as issue #2448 calls it (out and lse are
+ * inputs; dropout 0; no bias; deterministic).
+ */
+int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                    int batch, int total_q, int total_kv, int max_seqlen_q,
+                    int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                    int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Synchronises `stream`, then copies the device status word of the last call that
+ * used `workspace` into *status (0 = clean, else TE_STATUS_* bits). Returns TE_OK or
+ * TE_ERR_CUDA. Intended for tests and debugging; it blocks the host.
+ */
+int te_attn_read_status(const void* workspace, int* status, void* stream);
+
+/* Thread-local description of the last error returned on this thread. */
+const char* te_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TE_ATTN_H_ */

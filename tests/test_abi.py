@@ -1,0 +1,76 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU, exports
+every function include/te_attn.h declares, and its host-only helpers answer."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "te_attn.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(te_attn_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import bwd_packed_varlen_gb300 as ta
+    if not os.path.exists(ta.library_path()):
+        from bwd_packed_varlen_gb300 import build
+        build.build()
+    return ta.library()
+
+
+def test_header_declares_the_two_entry_points():
+    names = _declared()
+    assert "te_attn_fwd_thd" in names and "te_attn_bwd_thd" in names
+    assert len(names) >= 7
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_host_helpers(lib):
+    import bwd_packed_varlen_gb300 as ta
+    assert ta.version() >= 10000
+    assert ta.fwd_workspace_size(7, 32960, 32960, 32, 8, 128) > 0
+    # backward workspace holds D = rowsum(dO * O): fp32 [total_q, hq]
+    assert (ta.bwd_workspace_size(7, 32960, 32960, 32, 8, 128)
+            - ta.fwd_workspace_size(7, 32960, 32960, 32, 8, 128)) >= 32960 * 32 * 4
+    assert ta.fwd_workspace_size(0, 10, 10, 2, 1, 64) == 0
+    assert lib.te_attn_last_error() is not None
+
+
+def test_no_cpu_path():
+    """The binding refuses CPU tensors instead of computing anything on the host."""
+    import torch
+    import bwd_packed_varlen_gb300 as ta
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises((ValueError, RuntimeError)):
+        ta.fwd(q, q, q, cu, cu, cu, cu, 0.1, 1)
+
+
+def _param_counts():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(te_attn_\w+)\s*\(([^)]*)\)\s*;", src):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    return out
+
+
+def test_binding_signatures_match_header(lib):
+    """Every ctypes prototype has as many parameters as the C declaration."""
+    counts = _param_counts()
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == n, (name, n, fn.argtypes)
