@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Throughput of THD attention forward + backward on GB300.
+
+One step = te_attn_fwd_thd + te_attn_bwd_thd over the large packed workload:
+32768 real tokens in seeded lengths in [256, 8192] (each padded to a multiple of
+64 rows in memory), GQA hq=32 / hkv=8, head_dim 128, padding_causal, bf16.
+The metric is causal-adjusted algorithmic fwd+bwd TFLOPS: per (sequence, query
+head) 3.5 * 4 * d * Lq*Lk/2 FLOPs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica of the workload on its own GPU
+(the path needs no collective); rank 0 prints one JSON line. ``--impl reference``
+times the CPU float64 oracle on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "THD attn fwd+bwd TFLOPS (causal-adj) & % GB300 dense BF16 peak, 1 GPU"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["throughput", "small"], default="throughput",
+                    help="small: the same recipe with 8192 real tokens (for ncu captures)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            raw = json.load(open(path))
+
+            def find(*keys):
+                for k in keys:
+                    if k in raw and isinstance(raw[k], (int, float)):
+                        return float(raw[k])
+                return None
+            out = {"hbm_gbs": find("hbm_gbs"), "bf16_tflops": find("bf16_tflops"),
+                   "bf16_tflops_sustained": find("bf16_tflops_sustained")}
+            if all(v is not None for v in out.values()):
+                out["source"] = "measured"
+                return out
+        except Exception:
+            pass
+    out = dict(FALLBACK)
+    out["source"] = "fallback"
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=10)
+        except Exception:
+            self.proc.kill()
+            text = ""
+        sm, smax, pw, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            if self.uuid and f[0] != self.uuid:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(pw)}
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bwd_packed_varlen_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        t = json.load(open(path))
+        if t.get("source_hash") != kernel_source_hash():
+            return None
+        return t.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch_full")
+    except Exception:
+        return None
+
+
+def causal_pairs(w):
+    import numpy as np
+    lq = np.diff(w.cu_seqlens_q.numpy()).astype(np.float64)
+    lk = np.diff(w.cu_seqlens_kv.numpy()).astype(np.float64)
+    f = 0.5 if w.mask_type == 2 else 1.0
+    return float((lq * lk * f).sum())
+
+
+def workload_config(w):
+    lengths = w.meta.get("lengths")
+    return {
+        "workload": (f"packed THD fwd+bwd: {sum(lengths)} real tokens in {len(lengths)} seeded "
+                     f"sequences {lengths} padded to multiples of 64 (T={w.q.shape[0]}), "
+                     f"hq={w.hq}, hkv={w.hkv}, d={w.d}, padding_causal, bf16"),
+        "global_batch": len(lengths),
+        "seq_len": max(lengths),
+        "total_tokens": int(sum(lengths)),
+        "padded_rows": int(w.q.shape[0]),
+        "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
+        "parallelism": "replicas (one independent workload per GPU)",
+        "l2": "flushed between timed steps (256 MiB write)",
+    }
+
+
+# ------------------------------------------------------------ oracle sample
+
+
+def oracle_sample(w, seqs, groups):
+    """Run the CPU float64 oracle on (sequence, kv-group) pairs of the workload;
+    returns (seconds, algorithmic FLOPs of the sample)."""
+    import numpy as np
+    import oracle
+    G = w.hq // w.hkv
+    cq, cp = w.cu_seqlens_q.numpy(), w.cu_seqlens_q_padded.numpy()
+    flops = 0.0
+    args = []
+    for b in seqs:
+        o, L = int(cp[b]), int(cq[b + 1] - cq[b])
+        for g in groups:
+            hs = slice(g * G, g * G + G)
+            args.append((w.q[o:o + L, hs].double().numpy(), w.k[o:o + L, g].double().numpy(),
+                         w.v[o:o + L, g].double().numpy(), w.dout[o:o + L, hs].double().numpy()))
+            flops += 3.5 * 4.0 * w.d * G * L * L / 2.0
+    t0 = time.perf_counter()
+    for q, k, v, do in args:
+        oracle.attn_group_fwd_bwd(q, k, v, do, w.attn_scale, True)
+    return time.perf_counter() - t0, flops
+
+
+def blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from bwd_packed_varlen_gb300 import workloads as W
+    w = W.throughput()
+    seqs, groups = [4], [0]
+    for _ in range(args.warmup):
+        oracle_sample(w, seqs, groups)
+    times, fl = [], 0.0
+    for _ in range(args.steps):
+        t, fl = oracle_sample(w, seqs, groups)
+        times.append(t)
+    mean = sum(times) / len(times)
+    val = fl / mean / 1e12
+    sample = (f"sequence 4 ({int(w.cu_seqlens_q[5] - w.cu_seqlens_q[4])} tokens) x kv-group 0 "
+              f"(4 query heads) of the workload, fwd+bwd")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import bwd_packed_varlen_gb300 as ta
+    from bwd_packed_varlen_gb300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    ta.library()
+    w = W.throughput() if args.workload == "throughput" else W.throughput(total=8192)
+    flops = w.algorithmic_flops()
+    pairs_h = causal_pairs(w) * w.hq  # sum over (sequence, query head) of Lq*Lk/2
+    t = {k: getattr(w, k).to(dev) for k in ("q", "k", "v", "dout", "cu_seqlens_q",
+                                             "cu_seqlens_kv", "cu_seqlens_q_padded",
+                                             "cu_seqlens_kv_padded")}
+    Tq, hq, d = w.q.shape
+    Tk, hkv, _ = w.k.shape
+    B = w.batch
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((Tq, hq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    wsf = torch.empty(ta.fwd_workspace_size(B, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ta.bwd_workspace_size(B, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cu = (t["cu_seqlens_q"], t["cu_seqlens_kv"], t["cu_seqlens_q_padded"], t["cu_seqlens_kv_padded"])
+
+    def step(q, k, v, do, cus):
+        ta.fwd(q, k, v, *cus, w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv,
+               out=out, lse=lse, workspace=wsf)
+        ta.bwd(q, k, v, out, do, lse, *cus, w.attn_scale, w.mask_type, w.max_seqlen_q,
+               w.max_seqlen_kv, dq=dq, dk=dk, dv=dv, workspace=wsb)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(t["q"], t["k"], t["v"], t["dout"], cu)
+    torch.cuda.synchronize()
+    ta.profile_read()  # clear
+
+    # ------------------------------------------------ device-resident timed region
+    ta.profile_enable(True)
+    clocks = ClockSampler(gpu_uuid(dev))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record()
+        step(t["q"], t["k"], t["v"], t["dout"], cu)
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ta.profile_enable(False)
+    kprof = ta.profile_read()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        x = torch.tensor([ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    value = world * flops / (ms * 1e-3) / 1e12
+    launches = sum(c for _, c in kprof.values())
+
+    # ------------------------------------------------ end to end from host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: v.pin_memory() for k, v in
+                   (("q", w.q), ("k", w.k), ("v", w.v), ("dout", w.dout),
+                    ("cu_seqlens_q", w.cu_seqlens_q), ("cu_seqlens_kv", w.cu_seqlens_kv),
+                    ("cu_seqlens_q_padded", w.cu_seqlens_q_padded),
+                    ("cu_seqlens_kv_padded", w.cu_seqlens_kv_padded))}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+        host_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (out, lse, dq, dk, dv)]
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            es[i].record()
+            for k_, v_ in host_in.items():
+                dev_in[k_].copy_(v_, non_blocking=True)
+            step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["dout"],
+                 (dev_in["cu_seqlens_q"], dev_in["cu_seqlens_kv"], dev_in["cu_seqlens_q_padded"],
+                  dev_in["cu_seqlens_kv_padded"]))
+            for ho, dx in zip(host_out, (out, lse, dq, dk, dv)):
+                ho.copy_(dx, non_blocking=True)
+            ee[i].record()
+        torch.cuda.synchronize()
+        barrier()
+        ems = sum(a.elapsed_time(b) for a, b in zip(es, ee)) / args.steps
+        if world > 1:
+            x = torch.tensor([ems], device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            ems = float(x.item())
+        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": ems, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        return
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks = load_peaks()
+    credited = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 2.0 * d * pairs_h}
+    executed = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 6.0 * d * pairs_h}
+    kernels = {}
+    for name, (tot, cnt) in kprof.items():
+        if cnt == 0:
+            continue
+        avg = tot / cnt
+        ent = {"launches": cnt, "total_ms": tot, "avg_ms": avg, "share": tot / max(1e-9, sum(
+            x for x, _ in kprof.values()))}
+        if name in credited:
+            ent["tflops_credited"] = credited[name] / (avg * 1e-3) / 1e12
+            ent["tflops_executed"] = executed[name] / (avg * 1e-3) / 1e12
+        kernels[name] = ent
+    dom = max(("fwd", "dkdv", "dq"), key=lambda n: kernels.get(n, {}).get("total_ms", 0.0))
+    peak = peaks["bf16_tflops_sustained"]
+    ach = kernels[dom]["tflops_credited"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": ncu_traffic(dom),
+                "peak_kind": f"bf16 dense sustained ({peaks['source']})",
+                "flops_per_launch": credited[dom]}
+    if "delta" in kernels:
+        dbytes = 2 * Tq * hq * d * 2 + Tq * hq * 4
+        kernels["delta"]["gbs"] = dbytes / (kernels["delta"]["avg_ms"] * 1e-3) / 1e9
+        kernels["delta"]["hbm_frac"] = kernels["delta"]["gbs"] / peaks["hbm_gbs"]
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1 and args.workload == "throughput":
+        secs, fl = oracle_sample(w, [3, 4], [0, 1, 2])
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOPS", "cores": blas_threads(),
+               "kind": "oracle", "seconds": secs,
+               "sample": "sequences 3 and 4 (6668 and 3977 tokens) x kv-groups 0-2 (4 query "
+                         "heads each) of the workload, fwd+bwd, numpy float64"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "pct_peak": {"burst": value / world / peaks["bf16_tflops"],
+                     "sustained": value / world / peaks["bf16_tflops_sustained"],
+                     "source": peaks["source"]},
+        "flops_per_step": flops * world,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk, "kernels": kernels, "step_ms_min": min(step_ms),
+        "step_ms_max": max(step_ms),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
