@@ -13,6 +13,9 @@ from ._binding import (  # noqa: F401
     bwd,
     fwd,
     fwd_workspace_size,
+    KERNELS,
+    profile_enable,
+    profile_read,
     bwd_workspace_size,
     library,
     library_path,

@@ -60,6 +60,10 @@ def library() -> ctypes.CDLL:
     L.te_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     L.te_attn_last_error.restype = ctypes.c_char_p
     L.te_attn_last_error.argtypes = []
+    L.te_attn_profile_enable.restype = i32
+    L.te_attn_profile_enable.argtypes = [i32]
+    L.te_attn_profile_read.restype = i32
+    L.te_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
     _lib = L
     return L
 
@@ -180,3 +184,20 @@ def read_status(workspace, stream=None) -> int:
     val = ctypes.c_int(0)
     _check(L.te_attn_read_status(_ptr(workspace), ctypes.byref(val), ctypes.c_void_p(st)))
     return int(val.value)
+
+
+KERNELS = ("schedule", "fwd", "zero_fill", "delta", "dkdv", "dq")
+
+
+def profile_enable(on: bool = True) -> None:
+    """Bracket every later launch with CUDA events on its stream (te_attn_profile_enable)."""
+    _check(library().te_attn_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """Per-kernel ``{name: (total_ms, launches)}`` since the last read (te_attn_profile_read)."""
+    n = len(KERNELS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    _check(library().te_attn_profile_read(ms, cnt))
+    return {KERNELS[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}

@@ -69,23 +69,36 @@ __device__ __forceinline__ void store_row32(elem_t<kBF16>* row, int c0, int d, c
 // ===========================================================================
 // dK / dV
 // ===========================================================================
+// Thread roles: warps 0-7 compute (warp w owns TMEM lanes 32*(w%4).. and the query
+// columns [32*(w/4), +32) of each 64-column step), warp 8 TMA, warp 9 MMA.
+// TMEM: dK at columns [0, kDo), dV at [128, 128+kDo), and two step buffers at
+// 256 and 384, each holding S^T (64 columns) then dP^T (64 columns); while the
+// compute warps turn buffer b into P^T / dS^T, the tensor cores fill the other.
+constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdThreads = (kBwdComputeWarps + 2) * 32;
+constexpr int kBwdComputeThreads = kBwdComputeWarps * 32;
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
 template <int kD>
 struct DkdvShape {
-  static constexpr int kBM = kD <= 128 ? 128 : 64;   // query rows per step
-  static constexpr int kSplit = kD <= 128 ? 1 : 2;   // output column halves
-  static constexpr int kDo = kD / kSplit;            // output columns per block
+  static constexpr int kBM = 64;                      // query rows per step
+  static constexpr int kSplit = kD <= 128 ? 1 : 2;    // output column halves
+  static constexpr int kDo = kD / kSplit;             // output columns per block (<= 128)
   static constexpr int kChunks = kD / 64;
-  static constexpr int kKVBytes = kChunks * 16384;   // one 128-row K or V tile
-  static constexpr int kQBytes = kChunks * kBM * 128; // one kBM-row Q or dO tile
-  static constexpr int kStages = (2 * kKVBytes + 4 * kQBytes + 4 * kBM * 4 + 2048 <= 227 * 1024) ? 2 : 1;
-  static constexpr int kSmemUsed = 2 * kKVBytes + kStages * 2 * kQBytes + kStages * 2 * kBM * 4 + 1024;
-  // At least 120 KB so that one block owns an SM (and all of TMEM).
+  static constexpr int kKVBytes = kChunks * 16384;    // one 128-row K or V tile
+  static constexpr int kQBytes = kChunks * kBM * 128; // one 64-row Q or dO tile
+  static constexpr int kStageBytes = 2 * kQBytes + 2 * kBM * 4;
+  static constexpr int kFixed = 2 * kKVBytes + 1024 + 2048;
+  static constexpr int kStages = cmin(4, (227 * 1024 - kFixed) / kStageBytes);
+  static constexpr int kSmemUsed = 2 * kKVBytes + kStages * kStageBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr uint32_t kColDK = 0, kColDV = 128, kColST = 256, kColDPT = 256 + kBM;
+  static constexpr uint32_t kColDK = 0, kColDV = 128, kColBuf = 256;
+  static_assert(kStages >= 1, "shared memory budget");
 };
 
 template <int kD, bool kBF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV) {
@@ -103,7 +116,7 @@ __global__ void __launch_bounds__(192, 1)
 
   __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_q_full[NS], bar_q_empty[NS];
-  __shared__ uint64_t bar_s_full, bar_ds_ready;
+  __shared__ uint64_t bar_s_full[2], bar_ds_ready[2];
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -116,16 +129,18 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&bar_kv_full, 1);
     mbar_init(&bar_kv_empty, 1);
     mbar_init(&bar_acc_full, 1);
-    mbar_init(&bar_acc_empty, 128);
+    mbar_init(&bar_acc_empty, kBwdComputeThreads);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&bar_q_full[i], 1 + 32);
+      mbar_init(&bar_q_full[i], 1);
       mbar_init(&bar_q_empty[i], 1);
     }
-    mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_ds_ready, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_ds_ready[i], kBwdComputeThreads);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -137,7 +152,7 @@ __global__ void __launch_bounds__(192, 1)
   // Per-item geometry, identical in every role.
   struct Item {
     SeqInfo s;
-    int kt, g, split, qt0, nq, steps;
+    int b, kt, g, split, qt0, nq, steps;
   };
   auto decode = [&](int item) {
     Item it;
@@ -146,6 +161,7 @@ __global__ void __launch_bounds__(192, 1)
     it.g = rem / S::kSplit;
     it.split = rem % S::kSplit;
     it.kt = pr.y;
+    it.b = pr.x;
     it.s = load_seq(p, pr.x);
     it.qt0 = causal ? (it.kt * kBlockN) / kBM : 0;
     it.nq = (it.s.len_q + kBM - 1) / kBM;
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(192, 1)
     return it;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------- producer
     int it = 0, ii = 0;
     bool ok = true;
@@ -186,25 +202,20 @@ __global__ void __launch_bounds__(192, 1)
           if (!ok) break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_q_full[st], 2 * S::kQBytes);
+          mbar_arrive_expect_tx(&bar_q_full[st], 2 * S::kQBytes + 2 * kBM * 4);
           for (int c = 0; c < S::kChunks; ++c) {
             tma_load_3d(sQ + st * S::kQBytes + c * kBM * 128, &tmQ, &bar_q_full[st], c * 64, h,
                         I.s.off_q + qt * kBM);
             tma_load_3d(sDO + st * S::kQBytes + c * kBM * 128, &tmDO, &bar_q_full[st], c * 64, h,
                         I.s.off_q + qt * kBM);
           }
+          const size_t ti = tiled_index(p, I.b, qt * kBM, h);
+          bulk_load(sLse + st * kBM, p.lse_t + ti, kBM * 4, &bar_q_full[st]);
+          bulk_load(sDelta + st * kBM, p.delta_t + ti, kBM * 4, &bar_q_full[st]);
         }
-        for (int r = lane; r < kBM; r += 32) {
-          const int row = qt * kBM + r;
-          const bool valid = row < I.s.len_q;
-          const size_t gi = static_cast<size_t>(I.s.off_q + row) * p.hq + h;
-          sLse[st * kBM + r] = valid ? p.lse_in[gi] * kLog2e : 0.f;
-          sDelta[st * kBM + r] = valid ? p.delta[gi] : 0.f;
-        }
-        mbar_arrive(&bar_q_full[st]);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
@@ -212,61 +223,77 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const uint32_t t_dk = tmem + S::kColDK, t_dv = tmem + S::kColDV;
-      const uint32_t t_st = tmem + S::kColST, t_dpt = tmem + S::kColDPT;
       int it = 0, ii = 0;
       bool ok = true;
+      // S^T = K Q^T and dP^T = V dO^T of global step `cur` into buffer cur & 1.
+      auto issue_sdp = [&](int cur) -> bool {
+        const int st = cur % NS;
+        if (!mbar_wait(&bar_q_full[st], (cur / NS) & 1, status)) return false;
+        tc_fence_after();
+        const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
+        const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
+#pragma unroll
+        for (int s = 0; s < kD / 16; ++s) {
+          const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
+          const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
+          mma_ss(buf, make_smem_desc(k_addr + ok_off, 16, 1024, kLayoutSW128),
+                 make_smem_desc(qb + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int s = 0; s < kD / 16; ++s) {
+          const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
+          const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
+          mma_ss(buf + 64, make_smem_desc(v_addr + ok_off, 16, 1024, kLayoutSW128),
+                 make_smem_desc(dob + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s_full[cur & 1]);
+        return true;
+      };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
         const Item I = decode(item);
         if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
         const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
-        for (int t = 0; t < I.steps; ++t, ++it) {
-          const int st = it % NS;
-          if (!(ok = mbar_wait(&bar_q_full[st], (it / NS) & 1, status))) break;
-          tc_fence_after();
-          const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
-#pragma unroll
-          for (int s = 0; s < kD / 16; ++s) {
-            const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
-            const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-            mma_ss(t_st, make_smem_desc(k_addr + ok_off, 16, 1024, kLayoutSW128),
-                   make_smem_desc(qb + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int s = 0; s < kD / 16; ++s) {
-            const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
-            const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-            mma_ss(t_dpt, make_smem_desc(v_addr + ok_off, 16, 1024, kLayoutSW128),
-                   make_smem_desc(dob + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar_s_full);
-          if (!(ok = mbar_wait(&bar_ds_ready, it & 1, status))) break;
+        if (!(ok = issue_sdp(it))) break;
+        for (int t = 0; t < I.steps; ++t) {
+          const int cur = it + t;
+          // Look one step ahead when a second Q/dO stage exists; with a single
+          // stage the next load must wait for this step's MMAs, so issue after them.
+          if (NS >= 2 && t + 1 < I.steps && !(ok = issue_sdp(cur + 1))) break;
+          if (!(ok = mbar_wait(&bar_ds_ready[cur & 1], (cur >> 1) & 1, status))) break;
           if (t == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
+          const int st = cur % NS;
+          const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
+          const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
 #pragma unroll
           for (int s = 0; s < kBM / 16; ++s) {
             const uint32_t acc = (t > 0 || s > 0) ? 1u : 0u;
-            mma_ts(t_dv, t_st + s * 8,
+            const uint32_t acol = (s >> 1) * 32 + (s & 1) * 8;
+            mma_ts(t_dv, buf + acol,
                    make_smem_desc(dob + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
-            mma_ts(t_dk, t_dpt + s * 8,
+            mma_ts(t_dk, buf + 64 + acol,
                    make_smem_desc(qb + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
           }
           mma_commit(&bar_q_empty[st]);
+          if (NS == 1 && t + 1 < I.steps && !(ok = issue_sdp(cur + 1))) break;
         }
         if (!ok) break;
+        it += I.steps;
         mma_commit(&bar_kv_empty);
         mma_commit(&bar_acc_full);
       }
     }
   } else {
     // ------------------------------------------------------------- compute
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_st = tmem + S::kColST + lane_base, t_dpt = tmem + S::kColDPT + lane_base;
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int col0 = half * 32;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
       const Item I = decode(item);
-      const int kv_row = I.kt * kBlockN + tid;
+      const int kv_row = I.kt * kBlockN + quarter * 32 + lane;
       const bool kv_valid = kv_row < I.s.len_k;
       const int nqt = I.nq - I.qt0;
       for (int t = 0; t < I.steps; ++t, ++it) {
@@ -274,42 +301,59 @@ __global__ void __launch_bounds__(192, 1)
         const int st = it % NS;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_full[st], (it / NS) & 1, status));
         if (!ok) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[it & 1], (it >> 1) & 1, status));
         if (!ok) break;
         tc_fence_after();
-        const float* lse2 = sLse + st * kBM;
-        const float* dlt = sDelta + st * kBM;
-        // query columns i with a nonzero P^T for this key row: [lo, hi)
-        const int q_base = qt * kBM;
-        const int hi = kv_valid ? min(kBM, I.s.len_q - q_base) : 0;
-        const int lo = causal ? max(0, kv_row - q_base) : 0;
+        const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
+        uint32_t sv[32], dv[32];
+        tmem_ld32(buf, sv);
+        tmem_ld32(buf + 64, dv);
+        tmem_ld_wait();
+        float lse2[32], dlt[32];
 #pragma unroll
-        for (int c = 0; c < kBM / 32; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(t_st + c * 32, sv);
-          tmem_ld32(t_dpt + c * 32, dv);
-          tmem_ld_wait();
-          uint32_t pp[16], dd[16];
+        for (int k = 0; k < 8; ++k) {
+          const float4 a = reinterpret_cast<const float4*>(sLse + st * kBM + col0)[k];
+          const float4 b = reinterpret_cast<const float4*>(sDelta + st * kBM + col0)[k];
+          lse2[4 * k] = a.x; lse2[4 * k + 1] = a.y; lse2[4 * k + 2] = a.z; lse2[4 * k + 3] = a.w;
+          dlt[4 * k] = b.x; dlt[4 * k + 1] = b.y; dlt[4 * k + 2] = b.z; dlt[4 * k + 3] = b.w;
+        }
+        // query columns i of this half with a nonzero P^T for this key row: [lo, hi)
+        const int q_base = qt * kBM + col0;
+        const int hi = kv_valid ? min(32, I.s.len_q - q_base) : 0;
+        const int lo = causal ? max(0, kv_row - q_base) : 0;
+        uint32_t pp[16], dd[16];
+        if (lo == 0 && hi >= 32) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int i0 = c * 32 + 2 * k, i1 = i0 + 1;
-            const bool m0 = i0 >= lo && i0 < hi, m1 = i1 >= lo && i1 < hi;
-            const float p0 = m0 ? ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2[i0])) : 0.f;
-            const float p1 = m1 ? ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2[i1])) : 0.f;
-            const float d0 = m0 ? p0 * (__uint_as_float(dv[2 * k]) - dlt[i0]) : 0.f;
-            const float d1 = m1 ? p1 * (__uint_as_float(dv[2 * k + 1]) - dlt[i1]) : 0.f;
+            const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2[2 * k]));
+            const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2[2 * k + 1]));
+            const float d0 = p0 * (__uint_as_float(dv[2 * k]) - dlt[2 * k]);
+            const float d1 = p1 * (__uint_as_float(dv[2 * k + 1]) - dlt[2 * k + 1]);
             pp[k] = pack2<kBF16>(p0, p1);
             dd[k] = pack2<kBF16>(d0, d1);
           }
-          tmem_st16(t_st + c * 16, pp);
-          tmem_st16(t_dpt + c * 16, dd);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i0 = 2 * k, i1 = i0 + 1;
+            const bool m0 = i0 >= lo && i0 < hi, m1 = i1 >= lo && i1 < hi;
+            const float p0 = m0 ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2[i0])) : 0.f;
+            const float p1 = m1 ? ex2b(fmaf(__uint_as_float(sv[i1]), sl2, -lse2[i1])) : 0.f;
+            const float d0 = m0 ? p0 * (__uint_as_float(dv[i0]) - dlt[i0]) : 0.f;
+            const float d1 = m1 ? p1 * (__uint_as_float(dv[i1]) - dlt[i1]) : 0.f;
+            pp[k] = pack2<kBF16>(p0, p1);
+            dd[k] = pack2<kBF16>(d0, d1);
+          }
         }
+        tmem_st16(buf, pp);
+        tmem_st16(buf + 64, dd);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_ds_ready);
+        mbar_arrive(&bar_ds_ready[it & 1]);
       }
       if (!ok) break;
-      // Epilogue: scale * dK and dV for rows some real query sees.
+      // Epilogue: scale * dK and dV for rows some real query sees; each half of the
+      // compute warps stores half of the columns.
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
@@ -318,16 +362,16 @@ __global__ void __launch_bounds__(192, 1)
                               (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
       elem_t<kBF16>* dv_row = static_cast<elem_t<kBF16>*>(p.dv) +
                               (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
-      const int col0 = I.split * S::kDo;
+      const int col_out = I.split * S::kDo;
 #pragma unroll
-      for (int c0 = 0; c0 < S::kDo; c0 += 32) {
+      for (int c0 = half * (S::kDo / 2); c0 < (half + 1) * (S::kDo / 2); c0 += 32) {
         uint32_t a[32], b[32];
         tmem_ld32(tmem + S::kColDK + lane_base + c0, a);
         tmem_ld32(tmem + S::kColDV + lane_base + c0, b);
         tmem_ld_wait();
         if (store) {
-          store_row32<kBF16>(dk_row, col0 + c0, p.d, a, p.scale);
-          store_row32<kBF16>(dv_row, col0 + c0, p.d, b, 1.0f);
+          store_row32<kBF16>(dk_row, col_out + c0, p.d, a, p.scale);
+          store_row32<kBF16>(dv_row, col_out + c0, p.d, b, 1.0f);
         }
       }
       tc_fence_before();
@@ -337,7 +381,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -347,20 +391,25 @@ __global__ void __launch_bounds__(192, 1)
 // ===========================================================================
 // dQ
 // ===========================================================================
+// Same role split as dK/dV: compute warp w owns query rows 32*(w%4).. and key
+// columns [32*(w/4), +32) of each 64-key step. TMEM: dQ at [0, kD) and two step
+// buffers (S then dP, 64 columns each) after it.
 template <int kD>
 struct DqShape {
-  static constexpr int kBN = kD <= 128 ? 128 : 64;   // key rows per step
+  static constexpr int kBN = 64;                       // key rows per step
   static constexpr int kChunks = kD / 64;
-  static constexpr int kQBytes = kChunks * 16384;    // 128-row Q or dO tile
-  static constexpr int kKVBytes = kChunks * kBN * 128;
-  static constexpr int kStages = (2 * kQBytes + 4 * kKVBytes + 2048 <= 227 * 1024) ? 2 : 1;
+  static constexpr int kQBytes = kChunks * 16384;      // 128-row Q or dO tile
+  static constexpr int kKVBytes = kChunks * kBN * 128; // 64-row K or V tile
+  static constexpr int kFixed = 2 * kQBytes + 1024 + 2048;
+  static constexpr int kStages = cmin(4, (227 * 1024 - kFixed) / (2 * kKVBytes));
   static constexpr int kSmemUsed = 2 * kQBytes + kStages * 2 * kKVBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr uint32_t kColDQ = 0, kColS = kD, kColDP = kD + kBN;
+  static constexpr uint32_t kColDQ = 0, kColBuf = kD <= 128 ? 128 : 256;
+  static_assert(kStages >= 1, "shared memory budget");
 };
 
 template <int kD, bool kBF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
@@ -376,7 +425,7 @@ __global__ void __launch_bounds__(192, 1)
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_kv_full[NS], bar_kv_empty[NS];
-  __shared__ uint64_t bar_s_full, bar_ds_ready;
+  __shared__ uint64_t bar_s_full[2], bar_ds_ready[2];
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -388,16 +437,18 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&bar_q_full, 1);
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_acc_full, 1);
-    mbar_init(&bar_acc_empty, 128);
+    mbar_init(&bar_acc_empty, kBwdComputeThreads);
     for (int i = 0; i < NS; ++i) {
       mbar_init(&bar_kv_full[i], 1);
       mbar_init(&bar_kv_empty[i], 1);
     }
-    mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_ds_ready, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_ds_ready[i], kBwdComputeThreads);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -406,7 +457,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
@@ -438,58 +489,73 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint32_t t_dq = tmem + S::kColDQ, t_s = tmem + S::kColS, t_dp = tmem + S::kColDP;
+      const uint32_t t_dq = tmem + S::kColDQ;
       int it = 0, ii = 0;
       bool ok = true;
+      // S = Q K^T and dP = dO V^T of global step `cur` into buffer cur & 1.
+      auto issue_sdp = [&](int cur) -> bool {
+        const int st = cur % NS;
+        if (!mbar_wait(&bar_kv_full[st], (cur / NS) & 1, status)) return false;
+        tc_fence_after();
+        const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
+        const uint32_t kb = k_addr + st * S::kKVBytes, vb = v_addr + st * S::kKVBytes;
+#pragma unroll
+        for (int s2 = 0; s2 < kD / 16; ++s2) {
+          const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+          const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
+          mma_ss(buf, make_smem_desc(q_addr + oq, 16, 1024, kLayoutSW128),
+                 make_smem_desc(kb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kD / 16; ++s2) {
+          const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+          const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
+          mma_ss(buf + 64, make_smem_desc(do_addr + oq, 16, 1024, kLayoutSW128),
+                 make_smem_desc(vb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s_full[cur & 1]);
+        return true;
+      };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
         const int2 pr = p.q_pairs[item / p.hq];
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
-        for (int j = 0; j < n; ++j, ++it) {
-          const int st = it % NS;
-          if (!(ok = mbar_wait(&bar_kv_full[st], (it / NS) & 1, status))) break;
-          tc_fence_after();
-          const uint32_t kb = k_addr + st * S::kKVBytes, vb = v_addr + st * S::kKVBytes;
-#pragma unroll
-          for (int s2 = 0; s2 < kD / 16; ++s2) {
-            const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-            const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-            mma_ss(t_s, make_smem_desc(q_addr + oq, 16, 1024, kLayoutSW128),
-                   make_smem_desc(kb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int s2 = 0; s2 < kD / 16; ++s2) {
-            const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-            const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-            mma_ss(t_dp, make_smem_desc(do_addr + oq, 16, 1024, kLayoutSW128),
-                   make_smem_desc(vb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar_s_full);
-          if (!(ok = mbar_wait(&bar_ds_ready, it & 1, status))) break;
+        if (!(ok = issue_sdp(it))) break;
+        for (int j = 0; j < n; ++j) {
+          const int cur = it + j;
+          if (NS >= 2 && j + 1 < n && !(ok = issue_sdp(cur + 1))) break;
+          if (!(ok = mbar_wait(&bar_ds_ready[cur & 1], (cur >> 1) & 1, status))) break;
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
+          const int st = cur % NS;
+          const uint32_t kb = k_addr + st * S::kKVBytes;
+          const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2) {
-            mma_ts(t_dq, t_s + s2 * 8, make_smem_desc(kb + s2 * 2048, kBN * 128, 1024, kLayoutSW128),
+            const uint32_t acol = (s2 >> 1) * 32 + (s2 & 1) * 8;
+            mma_ts(t_dq, buf + acol, make_smem_desc(kb + s2 * 2048, kBN * 128, 1024, kLayoutSW128),
                    idDQ, (j > 0 || s2 > 0) ? 1u : 0u);
           }
           mma_commit(&bar_kv_empty[st]);
+          if (NS == 1 && j + 1 < n && !(ok = issue_sdp(cur + 1))) break;
         }
         if (!ok) break;
+        it += n;
         mma_commit(&bar_q_empty);
         mma_commit(&bar_acc_full);
       }
     }
   } else {
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + S::kColS + lane_base, t_dp = tmem + S::kColDP + lane_base;
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int col0 = half * 32;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
@@ -498,38 +564,47 @@ __global__ void __launch_bounds__(192, 1)
       const int h = item % p.hq;
       const SeqInfo s = load_seq(p, pr.x);
       const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
-      const int row = pr.y * kBlockM + tid;
+      const int row = pr.y * kBlockM + quarter * 32 + lane;
       const bool row_valid = row < s.len_q;
       const size_t gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
-      const float lse2 = row_valid ? p.lse_in[gi] * kLog2e : 0.f;
-      const float dlt = row_valid ? p.delta[gi] : 0.f;
+      const size_t ti = tiled_index(p, pr.x, pr.y * kBlockM + quarter * 32 + lane, h);
+      const float lse2 = row_valid ? p.lse_t[ti] : 0.f;
+      const float dlt = row_valid ? p.delta_t[ti] : 0.f;
       const int lim = row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
       for (int j = 0; j < n; ++j, ++it) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[it & 1], (it >> 1) & 1, status));
         if (!ok) break;
         tc_fence_after();
-        const int nvalid = lim - j * kBN;
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(t_s + c * 32, sv);
-          tmem_ld32(t_dp + c * 32, dv);
-          tmem_ld_wait();
-          uint32_t dd[16];
+        const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
+        uint32_t sv[32], dv[32];
+        tmem_ld32(buf, sv);
+        tmem_ld32(buf + 64, dv);
+        tmem_ld_wait();
+        const int nvalid = lim - (j * kBN + col0);
+        uint32_t dd[16];
+        if (nvalid >= 32) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int i0 = c * 32 + 2 * k, i1 = i0 + 1;
-            const float p0 = i0 < nvalid ? ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2)) : 0.f;
-            const float p1 = i1 < nvalid ? ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2)) : 0.f;
-            const float d0 = i0 < nvalid ? p0 * (__uint_as_float(dv[2 * k]) - dlt) : 0.f;
-            const float d1 = i1 < nvalid ? p1 * (__uint_as_float(dv[2 * k + 1]) - dlt) : 0.f;
+            const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2));
+            const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2));
+            dd[k] = pack2<kBF16>(p0 * (__uint_as_float(dv[2 * k]) - dlt),
+                                 p1 * (__uint_as_float(dv[2 * k + 1]) - dlt));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i0 = 2 * k, i1 = i0 + 1;
+            const float p0 = i0 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2)) : 0.f;
+            const float p1 = i1 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i1]), sl2, -lse2)) : 0.f;
+            const float d0 = i0 < nvalid ? p0 * (__uint_as_float(dv[i0]) - dlt) : 0.f;
+            const float d1 = i1 < nvalid ? p1 * (__uint_as_float(dv[i1]) - dlt) : 0.f;
             dd[k] = pack2<kBF16>(d0, d1);
           }
-          tmem_st16(t_s + c * 16, dd);
         }
+        tmem_st16(buf, dd);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_ds_ready);
+        mbar_arrive(&bar_ds_ready[it & 1]);
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
@@ -537,7 +612,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + gi * p.d;
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
+      for (int c0 = half * (kD / 2); c0 < (half + 1) * (kD / 2); c0 += 32) {
         uint32_t a[32];
         tmem_ld32(tmem + S::kColDQ + lane_base + c0, a);
         tmem_ld_wait();
@@ -550,7 +625,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -574,7 +649,7 @@ static cudaError_t launch_dkdv_impl(const AttnParams& p, int num_sms, cudaStream
   if (e != cudaSuccess) return e;
   const long long max_items = static_cast<long long>(p.pair_cap_k) * p.hkv * S::kSplit;
   const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
-  kern<<<grid, 192, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
+  kern<<<grid, kBwdThreads, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
   return cudaGetLastError();
 }
 
@@ -592,7 +667,7 @@ static cudaError_t launch_dq_impl(const AttnParams& p, int num_sms, cudaStream_t
   if (e != cudaSuccess) return e;
   const long long max_items = static_cast<long long>(p.pair_cap_q) * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
-  kern<<<grid, 192, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
+  kern<<<grid, kBwdThreads, S::kSmemBytes, st>>>(p, tq, tdo, tk, tv);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,11 @@ struct AttnParams {
   void* dq;
   void* dk;
   void* dv;
-  float* delta;        // backward: rowsum(dO * O), [total_q, hq]
+  // Backward, per (query tile pair, head) blocks of 128 rows in the natural pair
+  // order (pair = pref_q[b] + row / 128): lse * log2(e) and D = rowsum(dO * O).
+  float* lse_t;
+  float* delta_t;
+  const int* pref_q;   // prefix sums of query tiles per sequence (scheduler output)
 
   const int* cu_q;
   const int* cu_kv;
@@ -86,6 +90,13 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
     s.len_k = 0;
   }
   return s;
+}
+
+// Index of (natural query-tile pair of row i of sequence b, head h, row in tile)
+// in the tiled lse / D buffers.
+__device__ __forceinline__ size_t tiled_index(const AttnParams& p, int b, int i, int h) {
+  const int pair = p.pref_q[b] + i / kBlockM;
+  return (static_cast<size_t>(pair) * p.hq + h) * kBlockM + (i % kBlockM);
 }
 
 // Number of key rows a query tile can see (upper-left causal: key j <= query i).

@@ -254,10 +254,13 @@ cudaError_t launch_zero_fill(const AttnParams& p, int mode, int num_sms, cudaStr
 }
 
 // ---------------------------------------------------------------------------
-// Preprocess: delta[r, h] = sum_c float(dO[r,h,c]) * float(O[r,h,c]) on computed
-// rows, 0 elsewhere. One warp per row; lanes read 16-byte chunks. When d/8
-// divides 32 the lanes of one head are contiguous and reduce by shuffles;
-// otherwise each lane owns whole heads. Both orders are fixed (deterministic).
+// Preprocess: for every row the backward tiles read (real query rows of
+// sequences with keys), D[r, h] = sum_c float(dO[r,h,c]) * float(O[r,h,c]) and
+// lse[r, h] * log2(e), written tile-major (one contiguous block of 128 rows per
+// (query tile, head)) so the backward kernels fetch a tile's values with one
+// bulk copy. One warp per row; lanes read 16-byte chunks. When d/8 divides 32 the
+// lanes of one head are contiguous and reduce by shuffles; otherwise each lane
+// owns whole heads. Both orders are fixed (deterministic).
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
@@ -276,13 +279,17 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
   const int lane = threadIdx.x & 31;
   const int cpr = p.d / 8;  // 16-byte chunks per head
   const int chunks = p.hq * cpr;
+  constexpr float kLog2e = 1.4426950408889634f;
   for (int r = gw; r < p.total_q; r += warps) {
+    const int b = seq_of_row(p.cu_q_pad, p.batch, r);
+    if (b < 0) continue;
+    const SeqInfo s = load_seq(p, b);
+    const int i = r - s.off_q;
+    if (i >= s.len_q || s.len_k == 0) continue;  // no tile reads this row
     const size_t row = static_cast<size_t>(r);
-    float* drow = p.delta + row * p.hq;
-    if (q_row_kind(p, r) != 1) {
-      for (int h = lane; h < p.hq; h += 32) drow[h] = 0.f;
-      continue;
-    }
+    const size_t t0 = tiled_index(p, b, i, 0);   // + h * 128 for head h
+    for (int h = lane; h < p.hq; h += 32)
+      p.lse_t[t0 + static_cast<size_t>(h) * kBlockM] = p.lse_in[row * p.hq + h] * kLog2e;
     const uint4* o = reinterpret_cast<const uint4*>(static_cast<const T*>(p.out_in) +
                                                     row * p.hq * p.d);
     const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) +
@@ -290,15 +297,16 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
     if (32 % cpr == 0) {
       for (int c0 = 0; c0 < chunks; c0 += 32) {
         int c = c0 + lane;
-        float s = c < chunks ? dot8<T>(o[c], g[c]) : 0.f;
-        for (int w = cpr >> 1; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-        if (c < chunks && (c % cpr) == 0) drow[c / cpr] = s;
+        float v = c < chunks ? dot8<T>(o[c], g[c]) : 0.f;
+        for (int w = cpr >> 1; w > 0; w >>= 1) v += __shfl_xor_sync(0xffffffffu, v, w);
+        if (c < chunks && (c % cpr) == 0)
+          p.delta_t[t0 + static_cast<size_t>(c / cpr) * kBlockM] = v;
       }
     } else {
       for (int h = lane; h < p.hq; h += 32) {
-        float s = 0.f;
-        for (int c = 0; c < cpr; ++c) s += dot8<T>(o[h * cpr + c], g[h * cpr + c]);
-        drow[h] = s;
+        float v = 0.f;
+        for (int c = 0; c < cpr; ++c) v += dot8<T>(o[h * cpr + c], g[h * cpr + c]);
+        p.delta_t[t0 + static_cast<size_t>(h) * kBlockM] = v;
       }
     }
   }

@@ -11,7 +11,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/te_attn.h"
 #include "common.cuh"
@@ -34,7 +36,7 @@ int ok_status() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t header, pref_q, pref_k, q_pairs, k_pairs, delta, total;
+  size_t header, pref_q, pref_k, q_pairs, k_pairs, lse_t, delta_t, total;
   int cap_q, cap_k;
 };
 
@@ -44,7 +46,8 @@ struct Layout {
 //   pref_k  int32[batch+1]   prefix sums of key tiles per sequence
 //   q_pairs int2[cap_q]      sorted (sequence, query tile)
 //   k_pairs int2[cap_k]      sorted (sequence, key tile)
-//   delta   fp32[total_q*hq] backward only: rowsum(dO * O)
+//   lse_t   fp32[cap_q*hq*128] backward only: lse * log2(e), tile-major
+//   delta_t fp32[cap_q*hq*128] backward only: rowsum(dO * O), tile-major
 bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L) {
   if (batch < 1 || total_q < 0 || total_kv < 0 || hq < 1) return false;
   // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
@@ -64,8 +67,11 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   off = align_up(off + static_cast<size_t>(cq) * sizeof(int2), 256);
   L->k_pairs = off;
   off = align_up(off + static_cast<size_t>(ck) * sizeof(int2), 256);
-  L->delta = off;
-  if (backward) off = align_up(off + static_cast<size_t>(total_q) * hq * sizeof(float), 256);
+  const size_t tiled = static_cast<size_t>(cq) * hq * teattn::kBlockM * sizeof(float);
+  L->lse_t = off;
+  if (backward) off = align_up(off + tiled, 256);
+  L->delta_t = off;
+  if (backward) off = align_up(off + tiled, 256);
   L->total = off;
   return true;
 }
@@ -141,6 +147,33 @@ int cuda_fail(cudaError_t e, const char* where) {
   return fail(TE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
 }
 
+// Optional per-launch event timing (te_attn_profile_enable / _read).
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+
+// Runs `launch` between two events on `st` when profiling is enabled.
+template <typename F>
+cudaError_t timed(int kernel, cudaStream_t st, F&& launch) {
+  if (!g_prof_on) return launch();
+  ProfRecord r{kernel, nullptr, nullptr};
+  cudaError_t e = cudaEventCreate(&r.start);
+  if (e == cudaSuccess) e = cudaEventCreate(&r.stop);
+  if (e == cudaSuccess) e = cudaEventRecord(r.start, st);
+  if (e != cudaSuccess) return e;
+  e = launch();
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(r.stop, st);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.push_back(r);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,14 +231,14 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
   const bool bf16 = dtype == TE_DTYPE_BF16;
-  cudaError_t e = teattn::launch_schedule(p, pref_q, pref_k, st);
+  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   if (total_q > 0 && total_kv > 0) {
-    e = teattn::launch_attn_fwd(p, bf16, sms, st);
+    e = timed(TE_KERNEL_FWD, st, [&] { return teattn::launch_attn_fwd(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attention forward");
   }
   if (total_q > 0) {
-    e = teattn::launch_zero_fill(p, 0, sms, st);
+    e = timed(TE_KERNEL_ZERO_FILL, st, [&] { return teattn::launch_zero_fill(p, 0, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "zero fill");
   }
   return ok_status();
@@ -251,23 +284,25 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
   p.dk = dk;
   p.dv = dv;
   char* ws = static_cast<char*>(workspace);
-  p.delta = reinterpret_cast<float*>(ws + L.delta);
+  p.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
+  p.delta_t = reinterpret_cast<float*>(ws + L.delta_t);
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
+  p.pref_q = pref_q;
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
   const bool bf16 = dtype == TE_DTYPE_BF16;
-  cudaError_t e = teattn::launch_schedule(p, pref_q, pref_k, st);
+  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   if (total_q > 0) {
-    e = teattn::launch_delta(p, bf16, sms, st);
+    e = timed(TE_KERNEL_DELTA, st, [&] { return teattn::launch_delta(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "delta");
   }
   if (total_q > 0 && total_kv > 0) {
-    e = teattn::launch_attn_bwd_dkdv(p, bf16, sms, st);
+    e = timed(TE_KERNEL_DKDV, st, [&] { return teattn::launch_attn_bwd_dkdv(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "dK/dV");
-    e = teattn::launch_attn_bwd_dq(p, bf16, sms, st);
+    e = timed(TE_KERNEL_DQ, st, [&] { return teattn::launch_attn_bwd_dq(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "dQ");
   }
-  e = teattn::launch_zero_fill(p, 1, sms, st);
+  e = timed(TE_KERNEL_ZERO_FILL, st, [&] { return teattn::launch_zero_fill(p, 1, sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "zero fill");
   return ok_status();
 }
@@ -280,6 +315,39 @@ int te_attn_read_status(const void* workspace, int* status, void* stream) {
   e = cudaMemcpy(status, static_cast<const char*>(workspace), sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status copy");
   return ok_status();
+}
+
+int te_attn_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+  return ok_status();
+}
+
+int te_attn_profile_read(double* total_ms, int* launches) {
+  if (!total_ms || !launches) return fail(TE_ERR_INVALID_ARG, "NULL argument");
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  for (int k = 0; k < TE_NUM_KERNELS; ++k) {
+    total_ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  int rc = TE_OK;
+  for (ProfRecord& r : recs) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) rc = cuda_fail(e, "profile read");
+    if (r.kernel >= 0 && r.kernel < TE_NUM_KERNELS) {
+      total_ms[r.kernel] += ms;
+      launches[r.kernel] += 1;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  return rc == TE_OK ? ok_status() : rc;
 }
 
 const char* te_attn_last_error(void) { return g_last_error.c_str(); }
