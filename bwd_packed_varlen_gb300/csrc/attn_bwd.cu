@@ -66,17 +66,38 @@ __device__ __forceinline__ void store_row32(elem_t<kBF16>* row, int c0, int d, c
   }
 }
 
+// Store 16 fp32 values (scaled) as 16-bit to row[c0 .. c0+16), columns < d only.
+template <bool kBF16>
+__device__ __forceinline__ void store_row16(elem_t<kBF16>* row, int c0, int d, const uint32_t (&v)[16],
+                                            float scale) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int col = c0 + q * 8;
+    if (col + 8 <= d) {
+      uint4 w;
+      w.x = pack2<kBF16>(__uint_as_float(v[q * 8 + 0]) * scale, __uint_as_float(v[q * 8 + 1]) * scale);
+      w.y = pack2<kBF16>(__uint_as_float(v[q * 8 + 2]) * scale, __uint_as_float(v[q * 8 + 3]) * scale);
+      w.z = pack2<kBF16>(__uint_as_float(v[q * 8 + 4]) * scale, __uint_as_float(v[q * 8 + 5]) * scale);
+      w.w = pack2<kBF16>(__uint_as_float(v[q * 8 + 6]) * scale, __uint_as_float(v[q * 8 + 7]) * scale);
+      *reinterpret_cast<uint4*>(row + col) = w;
+    }
+  }
+}
+
 // ===========================================================================
 // dK / dV
 // ===========================================================================
-// Thread roles: warps 0-7 compute (warp w owns TMEM lanes 32*(w%4).. and the query
-// columns [32*(w/4), +32) of each 64-column step), warp 8 TMA, warp 9 MMA.
+// Thread roles: 16 compute warps (warp w owns TMEM lanes 32*(w%4).. and the 16 query
+// columns [16*(w/4), +16) of each 64-column step), then one TMA warp and one MMA warp.
 // TMEM: dK at columns [0, kDo), dV at [128, 128+kDo), and two step buffers at
 // 256 and 384, each holding S^T (64 columns) then dP^T (64 columns); while the
 // compute warps turn buffer b into P^T / dS^T, the tensor cores fill the other.
-constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdComputeWarps = 16;
 constexpr int kBwdThreads = (kBwdComputeWarps + 2) * 32;
 constexpr int kBwdComputeThreads = kBwdComputeWarps * 32;
+constexpr int kWarpProducer = kBwdComputeWarps, kWarpMma = kBwdComputeWarps + 1;
+constexpr int kColGroups = kBwdComputeWarps / 4;  // warps sharing one TMEM lane quarter
+constexpr int kGroupCols = 64 / kColGroups;       // step columns per compute warp
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -140,7 +161,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -169,7 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return it;
   };
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
     int it = 0, ii = 0;
     bool ok = true;
@@ -215,14 +236,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
       constexpr uint32_t idAcc = make_idesc_f16(kBF16, false, true, 128, S::kDo);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const uint32_t t_dk = tmem + S::kColDK, t_dv = tmem + S::kColDV;
+      // K, V, Q, dO K-major for S^T / dP^T; dO and Q N-major (d-contiguous) for dV / dK.
+      const SmemDesc dk = smem_desc(smem_u32(sK), 16, 1024, kLayoutSW128);
+      const SmemDesc dv = smem_desc(smem_u32(sV), 16, 1024, kLayoutSW128);
+      const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+      const SmemDesc ddo = smem_desc(smem_u32(sDO), 16, 1024, kLayoutSW128);
+      const SmemDesc dq_mn = smem_desc(smem_u32(sQ), kBM * 128, 1024, kLayoutSW128);
+      const SmemDesc ddo_mn = smem_desc(smem_u32(sDO), kBM * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
       // S^T = K Q^T and dP^T = V dO^T of global step `cur` into buffer cur & 1.
@@ -231,20 +257,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&bar_q_full[st], (cur / NS) & 1, status)) return false;
         tc_fence_after();
         const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
-        const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
+        const uint32_t so = (st * S::kQBytes) >> 4;
+        const SmemDesc qst{dq.lo + so, dq.hi}, dost{ddo.lo + so, ddo.hi};
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s) {
           const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
           const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-          mma_ss(buf, make_smem_desc(k_addr + ok_off, 16, 1024, kLayoutSW128),
-                 make_smem_desc(qb + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+          mma_ss(buf, dk, ok_off, qst, oq_off, idS, s > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s) {
           const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
           const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-          mma_ss(buf + 64, make_smem_desc(v_addr + ok_off, 16, 1024, kLayoutSW128),
-                 make_smem_desc(dob + oq_off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+          mma_ss(buf + 64, dv, ok_off, dost, oq_off, idS, s > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s_full[cur & 1]);
         return true;
@@ -263,16 +288,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (t == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           const int st = cur % NS;
-          const uint32_t qb = q_addr + st * S::kQBytes, dob = do_addr + st * S::kQBytes;
+          const uint32_t so = (st * S::kQBytes + split_off) >> 4;
+          const SmemDesc qst{dq_mn.lo + so, dq_mn.hi}, dost{ddo_mn.lo + so, ddo_mn.hi};
           const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
           for (int s = 0; s < kBM / 16; ++s) {
-            const uint32_t acc = (t > 0 || s > 0) ? 1u : 0u;
-            const uint32_t acol = (s >> 1) * 32 + (s & 1) * 8;
-            mma_ts(t_dv, buf + acol,
-                   make_smem_desc(dob + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
-            mma_ts(t_dk, buf + 64 + acol,
-                   make_smem_desc(qb + split_off + s * 2048, kBM * 128, 1024, kLayoutSW128), idAcc, acc);
+            const uint32_t acol = s * kGroupCols;  // 16 query rows packed by column group s
+            mma_ts(t_dv, buf + acol, dost, s * 2048, idAcc, s > 0 ? 1u : acc0);
+            mma_ts(t_dk, buf + 64 + acol, qst, s * 2048, idAcc, s > 0 ? 1u : acc0);
           }
           mma_commit(&bar_q_empty[st]);
           if (NS == 1 && t + 1 < I.steps && !(ok = issue_sdp(cur + 1))) break;
@@ -285,9 +309,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- compute
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int col0 = half * 32;
+    const int col0 = grp * kGroupCols;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
@@ -305,26 +329,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
-        uint32_t sv[32], dv[32];
-        tmem_ld32(buf, sv);
-        tmem_ld32(buf + 64, dv);
-        tmem_ld_wait();
-        float lse2[32], dlt[32];
+        uint32_t sv[16], dv[16];
+        tmem_ld16(buf, sv);
+        tmem_ld16(buf + 64, dv);
+        float lse2[16], dlt[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const float4 a = reinterpret_cast<const float4*>(sLse + st * kBM + col0)[k];
           const float4 b = reinterpret_cast<const float4*>(sDelta + st * kBM + col0)[k];
           lse2[4 * k] = a.x; lse2[4 * k + 1] = a.y; lse2[4 * k + 2] = a.z; lse2[4 * k + 3] = a.w;
           dlt[4 * k] = b.x; dlt[4 * k + 1] = b.y; dlt[4 * k + 2] = b.z; dlt[4 * k + 3] = b.w;
         }
-        // query columns i of this half with a nonzero P^T for this key row: [lo, hi)
+        tmem_ld_wait();
+        // query columns i of this group with a nonzero P^T for this key row: [lo, hi)
         const int q_base = qt * kBM + col0;
-        const int hi = kv_valid ? min(32, I.s.len_q - q_base) : 0;
+        const int hi = kv_valid ? min(kGroupCols, I.s.len_q - q_base) : 0;
         const int lo = causal ? max(0, kv_row - q_base) : 0;
-        uint32_t pp[16], dd[16];
-        if (lo == 0 && hi >= 32) {
+        uint32_t pp[8], dd[8];
+        if (lo == 0 && hi >= kGroupCols) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < 8; ++k) {
             const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2[2 * k]));
             const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2[2 * k + 1]));
             const float d0 = p0 * (__uint_as_float(dv[2 * k]) - dlt[2 * k]);
@@ -334,7 +358,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < 8; ++k) {
             const int i0 = 2 * k, i1 = i0 + 1;
             const bool m0 = i0 >= lo && i0 < hi, m1 = i1 >= lo && i1 < hi;
             const float p0 = m0 ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2[i0])) : 0.f;
@@ -345,15 +369,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dd[k] = pack2<kBF16>(d0, d1);
           }
         }
-        tmem_st16(buf, pp);
-        tmem_st16(buf + 64, dd);
+        tmem_st8(buf, pp);
+        tmem_st8(buf + 64, dd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_ds_ready[it & 1]);
       }
       if (!ok) break;
-      // Epilogue: scale * dK and dV for rows some real query sees; each half of the
-      // compute warps stores half of the columns.
+      // Epilogue: scale * dK and dV for rows some real query sees; each column group
+      // of the compute warps stores a quarter of the columns.
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
@@ -363,15 +387,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       elem_t<kBF16>* dv_row = static_cast<elem_t<kBF16>*>(p.dv) +
                               (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
       const int col_out = I.split * S::kDo;
+      constexpr int kOutCols = S::kDo / kColGroups;
 #pragma unroll
-      for (int c0 = half * (S::kDo / 2); c0 < (half + 1) * (S::kDo / 2); c0 += 32) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + S::kColDK + lane_base + c0, a);
-        tmem_ld32(tmem + S::kColDV + lane_base + c0, b);
+      for (int c = 0; c < kOutCols; c += 16) {
+        const int c0 = grp * kOutCols + c;
+        uint32_t a[16], b[16];
+        tmem_ld16(tmem + S::kColDK + lane_base + c0, a);
+        tmem_ld16(tmem + S::kColDV + lane_base + c0, b);
         tmem_ld_wait();
         if (store) {
-          store_row32<kBF16>(dk_row, col_out + c0, p.d, a, p.scale);
-          store_row32<kBF16>(dv_row, col_out + c0, p.d, b, 1.0f);
+          store_row16<kBF16>(dk_row, col_out + c0, p.d, a, p.scale);
+          store_row16<kBF16>(dv_row, col_out + c0, p.d, b, 1.0f);
         }
       }
       tc_fence_before();
@@ -381,7 +407,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -448,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -457,7 +483,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
@@ -489,13 +515,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       const uint32_t t_dq = tmem + S::kColDQ;
+      // Q, dO, K, V K-major for S / dP; K N-major (d-contiguous) for dS K.
+      const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+      const SmemDesc ddo = smem_desc(smem_u32(sDO), 16, 1024, kLayoutSW128);
+      const SmemDesc dk = smem_desc(smem_u32(sK), 16, 1024, kLayoutSW128);
+      const SmemDesc dv = smem_desc(smem_u32(sV), 16, 1024, kLayoutSW128);
+      const SmemDesc dk_mn = smem_desc(smem_u32(sK), kBN * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
       // S = Q K^T and dP = dO V^T of global step `cur` into buffer cur & 1.
@@ -504,20 +534,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&bar_kv_full[st], (cur / NS) & 1, status)) return false;
         tc_fence_after();
         const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
-        const uint32_t kb = k_addr + st * S::kKVBytes, vb = v_addr + st * S::kKVBytes;
+        const uint32_t so = (st * S::kKVBytes) >> 4;
+        const SmemDesc kst{dk.lo + so, dk.hi}, vst{dv.lo + so, dv.hi};
 #pragma unroll
         for (int s2 = 0; s2 < kD / 16; ++s2) {
           const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
           const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-          mma_ss(buf, make_smem_desc(q_addr + oq, 16, 1024, kLayoutSW128),
-                 make_smem_desc(kb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+          mma_ss(buf, dq, oq, kst, okv, idS, s2 > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int s2 = 0; s2 < kD / 16; ++s2) {
           const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
           const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-          mma_ss(buf + 64, make_smem_desc(do_addr + oq, 16, 1024, kLayoutSW128),
-                 make_smem_desc(vb + okv, 16, 1024, kLayoutSW128), idS, s2 > 0 ? 1u : 0u);
+          mma_ss(buf + 64, ddo, oq, vst, okv, idS, s2 > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s_full[cur & 1]);
         return true;
@@ -535,13 +564,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           const int st = cur % NS;
-          const uint32_t kb = k_addr + st * S::kKVBytes;
+          const SmemDesc kst{dk_mn.lo + ((st * S::kKVBytes) >> 4), dk_mn.hi};
           const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2) {
-            const uint32_t acol = (s2 >> 1) * 32 + (s2 & 1) * 8;
-            mma_ts(t_dq, buf + acol, make_smem_desc(kb + s2 * 2048, kBN * 128, 1024, kLayoutSW128),
-                   idDQ, (j > 0 || s2 > 0) ? 1u : 0u);
+            const uint32_t acol = s2 * kGroupCols;  // 16 key rows packed by column group s2
+            mma_ts(t_dq, buf + acol, kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
           }
           mma_commit(&bar_kv_empty[st]);
           if (NS == 1 && j + 1 < n && !(ok = issue_sdp(cur + 1))) break;
@@ -553,9 +582,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int col0 = half * 32;
+    const int col0 = grp * kGroupCols;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
@@ -576,15 +605,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
-        uint32_t sv[32], dv[32];
-        tmem_ld32(buf, sv);
-        tmem_ld32(buf + 64, dv);
+        uint32_t sv[16], dv[16];
+        tmem_ld16(buf, sv);
+        tmem_ld16(buf + 64, dv);
         tmem_ld_wait();
         const int nvalid = lim - (j * kBN + col0);
-        uint32_t dd[16];
-        if (nvalid >= 32) {
+        uint32_t dd[8];
+        if (nvalid >= kGroupCols) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < 8; ++k) {
             const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2));
             const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2));
             dd[k] = pack2<kBF16>(p0 * (__uint_as_float(dv[2 * k]) - dlt),
@@ -592,7 +621,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < 8; ++k) {
             const int i0 = 2 * k, i1 = i0 + 1;
             const float p0 = i0 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2)) : 0.f;
             const float p1 = i1 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i1]), sl2, -lse2)) : 0.f;
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dd[k] = pack2<kBF16>(d0, d1);
           }
         }
-        tmem_st16(buf, dd);
+        tmem_st8(buf, dd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_ds_ready[it & 1]);
@@ -611,12 +640,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + gi * p.d;
+      constexpr int kOutCols = kD / kColGroups;
 #pragma unroll
-      for (int c0 = half * (kD / 2); c0 < (half + 1) * (kD / 2); c0 += 32) {
-        uint32_t a[32];
-        tmem_ld32(tmem + S::kColDQ + lane_base + c0, a);
+      for (int c = 0; c < kOutCols; c += 16) {
+        const int c0 = grp * kOutCols + c;
+        uint32_t a[16];
+        tmem_ld16(tmem + S::kColDQ + lane_base + c0, a);
         tmem_ld_wait();
-        if (row_valid) store_row32<kBF16>(dq_row, c0, p.d, a, p.scale);
+        if (row_valid) store_row16<kBF16>(dq_row, c0, p.d, a, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&bar_acc_empty);
@@ -625,7 +656,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);

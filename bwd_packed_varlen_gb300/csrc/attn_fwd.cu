@@ -140,7 +140,10 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBlockN);
       constexpr uint32_t idPV = make_idesc_f16(kBF16, false, true, 128, kD);
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      // Operand descriptors: Q and K K-major; V as the N-major (d-contiguous) B of P V.
+      const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+      const SmemDesc dk = smem_desc(smem_u32(sK), 16, 1024, kLayoutSW128);
+      const SmemDesc dv = smem_desc(smem_u32(sV), 16384, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
       auto issue_s = [&](int t) -> bool {
@@ -148,12 +151,11 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&bar_k_full[sk], (t / SK) & 1, status)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem + S::kColS0 + (t & 1) * kBlockN;
-        const uint32_t kb = k_addr + sk * S::kTileBytes;
+        const SmemDesc kst{dk.lo + ((sk * S::kTileBytes) >> 4), dk.hi};
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s) {
           const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-          mma_ss(d_tmem, make_smem_desc(q_addr + off, 16, 1024, kLayoutSW128),
-                 make_smem_desc(kb + off, 16, 1024, kLayoutSW128), idS, s > 0 ? 1u : 0u);
+          mma_ss(d_tmem, dq, off, kst, off, idS, s > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s_full[t & 1]);
         mma_commit(&bar_k_empty[sk]);
@@ -178,12 +180,11 @@ __global__ void __launch_bounds__(192, 1)
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_o_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           const uint32_t a_tmem = tmem + S::kColS0 + (cur & 1) * kBlockN;
-          const uint32_t vb = v_addr + sv * S::kTileBytes;
+          const SmemDesc vst{dv.lo + ((sv * S::kTileBytes) >> 4), dv.hi};
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-          for (int s = 0; s < kBlockN / 16; ++s) {
-            mma_ts(t_o, a_tmem + s * 8, make_smem_desc(vb + s * 2048, 16384, 1024, kLayoutSW128),
-                   idPV, (j > 0 || s > 0) ? 1u : 0u);
-          }
+          for (int s = 0; s < kBlockN / 16; ++s)
+            mma_ts(t_o, a_tmem + s * 8, vst, s * 2048, idPV, s > 0 ? 1u : acc0);
           mma_commit(&bar_v_empty[sv]);
           mma_commit(&bar_o_ready[cur & 1]);
         }

@@ -184,6 +184,21 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
   return d;
 }
 
+// A descriptor split in two 32-bit words. The start address lives in the low 14
+// bits of `lo` (address >> 4), so a byte offset `off` inside shared memory is
+// applied as lo + (off >> 4): no carry can reach bit 14 because shared-memory
+// addresses stay below 2^18 bytes. Issue loops keep one SmemDesc per operand
+// buffer and add compile-time offsets per MMA.
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SmemDesc smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
+  const uint64_t d = make_smem_desc(saddr, lbo_bytes, sbo_bytes, layout);
+  return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
 // Instruction descriptor for kind::f16: D fp32, A/B both bf16 (or both fp16),
 // a_mn / b_mn select MN-major (transposed) operands, M in {64,128}, N % 16 == 0.
 __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, bool a_mn, bool b_mn, int M,
@@ -206,6 +221,27 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Same with split descriptors plus byte offsets added to their start addresses.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SmemDesc a, uint32_t a_off, SmemDesc b,
+                                       uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n"
+      " mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc),
+      "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t b_off,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %5, 0;\n mov.b64 db, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
