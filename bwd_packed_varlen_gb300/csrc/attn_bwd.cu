@@ -87,34 +87,48 @@ __device__ __forceinline__ void store_row16(elem_t<kBF16>* row, int c0, int d, c
 // ===========================================================================
 // dK / dV
 // ===========================================================================
-// Thread roles: 16 compute warps (warp w owns TMEM lanes 32*(w%4).. and the 16 query
-// columns [16*(w/4), +16) of each 64-column step), then one TMA warp and one MMA warp.
-// TMEM: dK at columns [0, kDo), dV at [128, 128+kDo), and two step buffers at
-// 256 and 384, each holding S^T (64 columns) then dP^T (64 columns); while the
-// compute warps turn buffer b into P^T / dS^T, the tensor cores fill the other.
+// Thread roles: 16 compute warps (warp w owns TMEM lanes 32*(w%4).. and the query
+// columns [(kBM/4)*(w/4), +kBM/4) of each step), then one TMA warp and one MMA warp.
+// TMEM: dK at columns [0, kDo), dV at [128, 128+kDo), S^T at [256, 256+kBM) and
+// dP^T at [384, 384+kBM). Each step is one query tile of kBM rows; the MMA thread
+// issues  S^T_t, dP^T_t, | dV_t, S^T_t+1, dK_t, dP^T_t+1 | ...  so the tensor cores
+// compute dP^T_t while the compute warps turn S^T_t into P^T_t, and dV_t / S^T_t+1
+// while they turn dP^T_t into dS^T_t. P^T and dS^T are written as 16-bit values
+// over the first half of each warp's own column range of S^T / dP^T.
 constexpr int kBwdComputeWarps = 16;
 constexpr int kBwdThreads = (kBwdComputeWarps + 2) * 32;
 constexpr int kBwdComputeThreads = kBwdComputeWarps * 32;
 constexpr int kWarpProducer = kBwdComputeWarps, kWarpMma = kBwdComputeWarps + 1;
 constexpr int kColGroups = kBwdComputeWarps / 4;  // warps sharing one TMEM lane quarter
-constexpr int kGroupCols = 64 / kColGroups;       // step columns per compute warp
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
+// TMEM column (relative to a score buffer) of the packed 16-bit operand for
+// MMA k-step s (16 rows of the reduction dimension): group g = s / (G/16) of
+// width G = step / 4 keeps its packed values in the first G/2 columns of its own
+// range [g*G, g*G+G).
+template <int kStep>
+__device__ __forceinline__ constexpr uint32_t packed_col(int s) {
+  constexpr int G = kStep / kColGroups;  // columns per group
+  constexpr int per = G / 16;            // k-steps per group
+  return static_cast<uint32_t>((s / per) * G + (s % per) * 8);
+}
+
 template <int kD>
 struct DkdvShape {
-  static constexpr int kBM = 64;                      // query rows per step
-  static constexpr int kSplit = kD <= 128 ? 1 : 2;    // output column halves
-  static constexpr int kDo = kD / kSplit;             // output columns per block (<= 128)
+  static constexpr int kBM = kD <= 128 ? 128 : 64;   // query rows per step
+  static constexpr int kSplit = kD <= 128 ? 1 : 2;   // output column halves
+  static constexpr int kDo = kD / kSplit;            // output columns per block (<= 128)
   static constexpr int kChunks = kD / 64;
-  static constexpr int kKVBytes = kChunks * 16384;    // one 128-row K or V tile
-  static constexpr int kQBytes = kChunks * kBM * 128; // one 64-row Q or dO tile
+  static constexpr int kKVBytes = kChunks * 16384;   // one 128-row K or V tile
+  static constexpr int kQBytes = kChunks * kBM * 128; // one kBM-row Q or dO tile
   static constexpr int kStageBytes = 2 * kQBytes + 2 * kBM * 4;
   static constexpr int kFixed = 2 * kKVBytes + 1024 + 2048;
   static constexpr int kStages = cmin(4, (227 * 1024 - kFixed) / kStageBytes);
   static constexpr int kSmemUsed = 2 * kKVBytes + kStages * kStageBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr uint32_t kColDK = 0, kColDV = 128, kColBuf = 256;
+  static constexpr int kG = kBM / kColGroups;        // query columns per compute warp
+  static constexpr uint32_t kColDK = 0, kColDV = 128, kColST = 256, kColDPT = 384;
   static_assert(kStages >= 1, "shared memory budget");
 };
 
@@ -124,7 +138,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV) {
   using S = DkdvShape<kD>;
-  constexpr int kBM = S::kBM, NS = S::kStages;
+  constexpr int kBM = S::kBM, NS = S::kStages, kG = S::kG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_q_full[NS], bar_q_empty[NS];
-  __shared__ uint64_t bar_s_full[2], bar_ds_ready[2];
+  __shared__ uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -155,10 +169,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_q_full[i], 1);
       mbar_init(&bar_q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_ds_ready[i], kBwdComputeThreads);
-    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_p_ready, kBwdComputeThreads);
+    mbar_init(&bar_ds_ready, kBwdComputeThreads);
     fence_barrier_init();
   }
   if (warp == kWarpMma) {
@@ -192,37 +206,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
-    int it = 0, ii = 0;
-    bool ok = true;
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-    }
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
-      const Item I = decode(item);
-      if (ii > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv_empty, (ii - 1) & 1, status));
-        if (!ok) break;
-      }
-      if (lane == 0) {
+      int it = 0, ii = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+        const Item I = decode(item);
+        if (ii > 0 && !(ok = mbar_wait(&bar_kv_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * S::kKVBytes);
         for (int c = 0; c < S::kChunks; ++c) {
           tma_load_3d(sK + c * 16384, &tmK, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
           tma_load_3d(sV + c * 16384, &tmV, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
         }
-      }
-      const int nqt = I.nq - I.qt0;
-      for (int t = 0; t < I.steps; ++t, ++it) {
-        const int h = I.g * p.group + t / nqt;
-        const int qt = I.qt0 + t % nqt;
-        const int st = it % NS;
-        if (it >= NS) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_empty[st], ((it / NS) - 1) & 1, status));
-          if (!ok) break;
-        }
-        if (lane == 0) {
+        const int nqt = I.nq - I.qt0;
+        for (int t = 0; t < I.steps; ++t, ++it) {
+          const int h = I.g * p.group + t / nqt;
+          const int qt = I.qt0 + t % nqt;
+          const int st = it % NS;
+          if (it >= NS && !(ok = mbar_wait(&bar_q_empty[st], ((it / NS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_q_full[st], 2 * S::kQBytes + 2 * kBM * 4);
           for (int c = 0; c < S::kChunks; ++c) {
             tma_load_3d(sQ + st * S::kQBytes + c * kBM * 128, &tmQ, &bar_q_full[st], c * 64, h,
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
       constexpr uint32_t idAcc = make_idesc_f16(kBF16, false, true, 128, S::kDo);
       const uint32_t t_dk = tmem + S::kColDK, t_dv = tmem + S::kColDV;
+      const uint32_t t_st = tmem + S::kColST, t_dpt = tmem + S::kColDPT;
       // K, V, Q, dO K-major for S^T / dP^T; dO and Q N-major (d-contiguous) for dV / dK.
       const SmemDesc dk = smem_desc(smem_u32(sK), 16, 1024, kLayoutSW128);
       const SmemDesc dv = smem_desc(smem_u32(sV), 16, 1024, kLayoutSW128);
@@ -251,55 +256,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SmemDesc ddo_mn = smem_desc(smem_u32(sDO), kBM * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      // S^T = K Q^T and dP^T = V dO^T of global step `cur` into buffer cur & 1.
-      auto issue_sdp = [&](int cur) -> bool {
-        const int st = cur % NS;
-        if (!mbar_wait(&bar_q_full[st], (cur / NS) & 1, status)) return false;
-        tc_fence_after();
-        const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
-        const uint32_t so = (st * S::kQBytes) >> 4;
-        const SmemDesc qst{dq.lo + so, dq.hi}, dost{ddo.lo + so, ddo.hi};
+      auto wait_q = [&](int cur) { return mbar_wait(&bar_q_full[cur % NS], (cur / NS) & 1, status); };
+      // S^T = K Q^T (A: K tile, B: Q stage) or dP^T = V dO^T for global step `cur`.
+      auto issue_st = [&](int cur, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
+        const SmemDesc bst{b.lo + ((cur % NS) * S::kQBytes >> 4), b.hi};
 #pragma unroll
-        for (int s = 0; s < kD / 16; ++s) {
-          const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
-          const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-          mma_ss(buf, dk, ok_off, qst, oq_off, idS, s > 0 ? 1u : 0u);
-        }
+        for (int s = 0; s < kD / 16; ++s)
+          mma_ss(d_tmem, a, (s >> 2) * 16384 + (s & 3) * 32, bst, (s >> 2) * (kBM * 128) + (s & 3) * 32,
+                 idS, s > 0 ? 1u : 0u);
+        mma_commit(done);
+      };
+      // dV += P^T dO or dK += dS^T Q for global step `cur` (A from TMEM).
+      auto issue_acc = [&](int cur, uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t split_off,
+                           uint32_t acc0) {
+        const SmemDesc bst{b.lo + (((cur % NS) * S::kQBytes + split_off) >> 4), b.hi};
 #pragma unroll
-        for (int s = 0; s < kD / 16; ++s) {
-          const uint32_t ok_off = (s >> 2) * 16384 + (s & 3) * 32;
-          const uint32_t oq_off = (s >> 2) * (kBM * 128) + (s & 3) * 32;
-          mma_ss(buf + 64, dv, ok_off, dost, oq_off, idS, s > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar_s_full[cur & 1]);
-        return true;
+        for (int s = 0; s < kBM / 16; ++s)
+          mma_ts(d_tmem, a_tmem + packed_col<kBM>(s), bst, s * 2048, idAcc, s > 0 ? 1u : acc0);
       };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
         const Item I = decode(item);
         if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
         const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
-        if (!(ok = issue_sdp(it))) break;
+        if (!(ok = wait_q(it))) break;
+        tc_fence_after();
+        issue_st(it, t_st, dk, dq, &bar_s_full);
+        issue_st(it, t_dpt, dv, ddo, &bar_dp_full);
         for (int t = 0; t < I.steps; ++t) {
           const int cur = it + t;
-          // Look one step ahead when a second Q/dO stage exists; with a single
-          // stage the next load must wait for this step's MMAs, so issue after them.
-          if (NS >= 2 && t + 1 < I.steps && !(ok = issue_sdp(cur + 1))) break;
-          if (!(ok = mbar_wait(&bar_ds_ready[cur & 1], (cur >> 1) & 1, status))) break;
+          const bool more = t + 1 < I.steps;
+          if (!(ok = mbar_wait(&bar_p_ready, cur & 1, status))) break;
           if (t == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
-          const int st = cur % NS;
-          const uint32_t so = (st * S::kQBytes + split_off) >> 4;
-          const SmemDesc qst{dq_mn.lo + so, dq_mn.hi}, dost{ddo_mn.lo + so, ddo_mn.hi};
-          const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
-          const uint32_t acc0 = t > 0 ? 1u : 0u;
-#pragma unroll
-          for (int s = 0; s < kBM / 16; ++s) {
-            const uint32_t acol = s * kGroupCols;  // 16 query rows packed by column group s
-            mma_ts(t_dv, buf + acol, dost, s * 2048, idAcc, s > 0 ? 1u : acc0);
-            mma_ts(t_dk, buf + 64 + acol, qst, s * 2048, idAcc, s > 0 ? 1u : acc0);
+          issue_acc(cur, t_dv, t_st, ddo_mn, split_off, t > 0 ? 1u : 0u);
+          if (NS >= 2 && more) {
+            if (!(ok = wait_q(cur + 1))) break;
+            tc_fence_after();
+            issue_st(cur + 1, t_st, dk, dq, &bar_s_full);
           }
-          mma_commit(&bar_q_empty[st]);
-          if (NS == 1 && t + 1 < I.steps && !(ok = issue_sdp(cur + 1))) break;
+          if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
+          tc_fence_after();
+          issue_acc(cur, t_dk, t_dpt, dq_mn, split_off, t > 0 ? 1u : 0u);
+          mma_commit(&bar_q_empty[cur % NS]);
+          if (more) {
+            if (NS == 1) {
+              if (!(ok = wait_q(cur + 1))) break;
+              tc_fence_after();
+              issue_st(cur + 1, t_st, dk, dq, &bar_s_full);
+            }
+            issue_st(cur + 1, t_dpt, dv, ddo, &bar_dp_full);
+          }
         }
         if (!ok) break;
         it += I.steps;
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------- compute
     const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int col0 = grp * kGroupCols;
+    const int col0 = grp * kG;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
@@ -325,55 +331,89 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = it % NS;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_full[st], (it / NS) & 1, status));
         if (!ok) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[it & 1], (it >> 1) & 1, status));
+        // query columns i of this warp with a nonzero P^T for this key row: [lo, hi)
+        const int q_base = qt * kBM + col0;
+        const int hi = kv_valid ? min(kG, I.s.len_q - q_base) : 0;
+        const int lo = causal ? max(0, kv_row - q_base) : 0;
+        // Warp-uniform: only tiles on the causal diagonal or a length boundary pay
+        // for per-element masking.
+        const bool full = __all_sync(0xffffffffu, lo == 0 && hi >= kG);
+        const float4* lse4 = reinterpret_cast<const float4*>(sLse + st * kBM + col0);
+        const float4* dlt4 = reinterpret_cast<const float4*>(sDelta + st * kBM + col0);
+        // ---- phase A: P^T = exp2(S^T * scale * log2e - lse2), masked entries 0
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
-        uint32_t sv[16], dv[16];
-        tmem_ld16(buf, sv);
-        tmem_ld16(buf + 64, dv);
-        float lse2[16], dlt[16];
+        float pv[kG];
+        {
+          uint32_t sv[kG];
+          if constexpr (kG == 32) tmem_ld32(tmem + S::kColST + lane_base + col0, sv);
+          else tmem_ld16(tmem + S::kColST + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(sv));
+          tmem_ld_wait();
+          if (full) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 a = reinterpret_cast<const float4*>(sLse + st * kBM + col0)[k];
-          const float4 b = reinterpret_cast<const float4*>(sDelta + st * kBM + col0)[k];
-          lse2[4 * k] = a.x; lse2[4 * k + 1] = a.y; lse2[4 * k + 2] = a.z; lse2[4 * k + 3] = a.w;
-          dlt[4 * k] = b.x; dlt[4 * k + 1] = b.y; dlt[4 * k + 2] = b.z; dlt[4 * k + 3] = b.w;
-        }
-        tmem_ld_wait();
-        // query columns i of this group with a nonzero P^T for this key row: [lo, hi)
-        const int q_base = qt * kBM + col0;
-        const int hi = kv_valid ? min(kGroupCols, I.s.len_q - q_base) : 0;
-        const int lo = causal ? max(0, kv_row - q_base) : 0;
-        uint32_t pp[8], dd[8];
-        if (lo == 0 && hi >= kGroupCols) {
+            for (int k = 0; k < kG / 4; ++k) {
+              const float4 l4 = lse4[k];
+              pv[4 * k] = ex2b(fmaf(__uint_as_float(sv[4 * k]), sl2, -l4.x));
+              pv[4 * k + 1] = ex2b(fmaf(__uint_as_float(sv[4 * k + 1]), sl2, -l4.y));
+              pv[4 * k + 2] = ex2b(fmaf(__uint_as_float(sv[4 * k + 2]), sl2, -l4.z));
+              pv[4 * k + 3] = ex2b(fmaf(__uint_as_float(sv[4 * k + 3]), sl2, -l4.w));
+            }
+          } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2[2 * k]));
-            const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2[2 * k + 1]));
-            const float d0 = p0 * (__uint_as_float(dv[2 * k]) - dlt[2 * k]);
-            const float d1 = p1 * (__uint_as_float(dv[2 * k + 1]) - dlt[2 * k + 1]);
-            pp[k] = pack2<kBF16>(p0, p1);
-            dd[k] = pack2<kBF16>(d0, d1);
+            for (int k = 0; k < kG / 4; ++k) {
+              const float4 l4 = lse4[k];
+              const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 4 * k + e;
+                const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -l[e]));
+                pv[i] = (i >= lo && i < hi) ? x : 0.f;
+              }
+            }
           }
-        } else {
+          uint32_t pk[kG / 2];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int i0 = 2 * k, i1 = i0 + 1;
-            const bool m0 = i0 >= lo && i0 < hi, m1 = i1 >= lo && i1 < hi;
-            const float p0 = m0 ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2[i0])) : 0.f;
-            const float p1 = m1 ? ex2b(fmaf(__uint_as_float(sv[i1]), sl2, -lse2[i1])) : 0.f;
-            const float d0 = m0 ? p0 * (__uint_as_float(dv[i0]) - dlt[i0]) : 0.f;
-            const float d1 = m1 ? p1 * (__uint_as_float(dv[i1]) - dlt[i1]) : 0.f;
-            pp[k] = pack2<kBF16>(p0, p1);
-            dd[k] = pack2<kBF16>(d0, d1);
-          }
+          for (int k = 0; k < kG / 2; ++k) pk[k] = pack2<kBF16>(pv[2 * k], pv[2 * k + 1]);
+          if constexpr (kG == 32) tmem_st16(tmem + S::kColST + lane_base + col0, pk);
+          else tmem_st8(tmem + S::kColST + lane_base + col0, *reinterpret_cast<uint32_t(*)[8]>(pk));
         }
-        tmem_st8(buf, pp);
-        tmem_st8(buf + 64, dd);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_ds_ready[it & 1]);
+        mbar_arrive(&bar_p_ready);
+        // ---- phase B: dS^T = P^T (dP^T - D)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_dp_full, it & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t dv[kG];
+          if constexpr (kG == 32) tmem_ld32(tmem + S::kColDPT + lane_base + col0, dv);
+          else tmem_ld16(tmem + S::kColDPT + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(dv));
+          tmem_ld_wait();
+          // Masked entries are selected to 0 (not multiplied): D of rows past the
+          // query length is never written and may hold any bits.
+          float r[kG];
+#pragma unroll
+          for (int k = 0; k < kG / 4; ++k) {
+            const float4 d4 = dlt4[k];
+            r[4 * k] = pv[4 * k] * (__uint_as_float(dv[4 * k]) - d4.x);
+            r[4 * k + 1] = pv[4 * k + 1] * (__uint_as_float(dv[4 * k + 1]) - d4.y);
+            r[4 * k + 2] = pv[4 * k + 2] * (__uint_as_float(dv[4 * k + 2]) - d4.z);
+            r[4 * k + 3] = pv[4 * k + 3] * (__uint_as_float(dv[4 * k + 3]) - d4.w);
+          }
+          if (!full) {
+#pragma unroll
+            for (int i = 0; i < kG; ++i) r[i] = (i >= lo && i < hi) ? r[i] : 0.f;
+          }
+          uint32_t dk[kG / 2];
+#pragma unroll
+          for (int k = 0; k < kG / 2; ++k) dk[k] = pack2<kBF16>(r[2 * k], r[2 * k + 1]);
+          if constexpr (kG == 32) tmem_st16(tmem + S::kColDPT + lane_base + col0, dk);
+          else tmem_st8(tmem + S::kColDPT + lane_base + col0, *reinterpret_cast<uint32_t(*)[8]>(dk));
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_ds_ready);
       }
       if (!ok) break;
       // Epilogue: scale * dK and dV for rows some real query sees; each column group
@@ -418,19 +458,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // dQ
 // ===========================================================================
 // Same role split as dK/dV: compute warp w owns query rows 32*(w%4).. and key
-// columns [32*(w/4), +32) of each 64-key step. TMEM: dQ at [0, kD) and two step
-// buffers (S then dP, 64 columns each) after it.
+// columns [(kBN/4)*(w/4), +kBN/4) of each step. TMEM: dQ at [0, kD), S at kColS,
+// dP at kColS + 128. The MMA thread issues  S_j, dP_j, | S_j+1, dQ_j, dP_j+1 | ...:
+// S_j+1 goes out as soon as the compute warps have read S_j into registers, dQ_j
+// once they have written dS_j (over their half of dP_j), dP_j+1 after dQ_j.
 template <int kD>
 struct DqShape {
-  static constexpr int kBN = 64;                       // key rows per step
+  static constexpr int kBN = kD <= 128 ? 128 : 64;     // key rows per step
   static constexpr int kChunks = kD / 64;
   static constexpr int kQBytes = kChunks * 16384;      // 128-row Q or dO tile
-  static constexpr int kKVBytes = kChunks * kBN * 128; // 64-row K or V tile
+  static constexpr int kKVBytes = kChunks * kBN * 128; // kBN-row K or V tile
   static constexpr int kFixed = 2 * kQBytes + 1024 + 2048;
   static constexpr int kStages = cmin(4, (227 * 1024 - kFixed) / (2 * kKVBytes));
   static constexpr int kSmemUsed = 2 * kQBytes + kStages * 2 * kKVBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
-  static constexpr uint32_t kColDQ = 0, kColBuf = kD <= 128 ? 128 : 256;
+  static constexpr int kG = kBN / kColGroups;          // key columns per compute warp
+  static constexpr uint32_t kColDQ = 0, kColS = kD <= 128 ? 128 : 256, kColDP = kColS + 128;
   static_assert(kStages >= 1, "shared memory budget");
 };
 
@@ -440,7 +483,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
   using S = DqShape<kD>;
-  constexpr int kBN = S::kBN, NS = S::kStages;
+  constexpr int kBN = S::kBN, NS = S::kStages, kG = S::kG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -451,7 +494,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_kv_full[NS], bar_kv_empty[NS];
-  __shared__ uint64_t bar_s_full[2], bar_ds_ready[2];
+  __shared__ uint64_t bar_s_full, bar_dp_full, bar_s_free, bar_ds_ready;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -468,10 +511,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_kv_full[i], 1);
       mbar_init(&bar_kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_ds_ready[i], kBwdComputeThreads);
-    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_s_free, kBwdComputeThreads);
+    mbar_init(&bar_ds_ready, kBwdComputeThreads);
     fence_barrier_init();
   }
   if (warp == kWarpMma) {
@@ -519,7 +562,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
-      const uint32_t t_dq = tmem + S::kColDQ;
+      const uint32_t t_dq = tmem + S::kColDQ, t_s = tmem + S::kColS, t_dp = tmem + S::kColDP;
       // Q, dO, K, V K-major for S / dP; K N-major (d-contiguous) for dS K.
       const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
       const SmemDesc ddo = smem_desc(smem_u32(sDO), 16, 1024, kLayoutSW128);
@@ -528,52 +571,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SmemDesc dk_mn = smem_desc(smem_u32(sK), kBN * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      // S = Q K^T and dP = dO V^T of global step `cur` into buffer cur & 1.
-      auto issue_sdp = [&](int cur) -> bool {
-        const int st = cur % NS;
-        if (!mbar_wait(&bar_kv_full[st], (cur / NS) & 1, status)) return false;
-        tc_fence_after();
-        const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
-        const uint32_t so = (st * S::kKVBytes) >> 4;
-        const SmemDesc kst{dk.lo + so, dk.hi}, vst{dv.lo + so, dv.hi};
+      auto wait_kv = [&](int cur) { return mbar_wait(&bar_kv_full[cur % NS], (cur / NS) & 1, status); };
+      // S = Q K^T (a = Q, b = K stage) or dP = dO V^T (a = dO, b = V stage) for step `cur`.
+      auto issue_s = [&](int cur, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
+        const SmemDesc bst{b.lo + ((cur % NS) * S::kKVBytes >> 4), b.hi};
 #pragma unroll
-        for (int s2 = 0; s2 < kD / 16; ++s2) {
-          const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-          const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-          mma_ss(buf, dq, oq, kst, okv, idS, s2 > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < kD / 16; ++s2) {
-          const uint32_t oq = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-          const uint32_t okv = (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32;
-          mma_ss(buf + 64, ddo, oq, vst, okv, idS, s2 > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar_s_full[cur & 1]);
-        return true;
+        for (int s2 = 0; s2 < kD / 16; ++s2)
+          mma_ss(d_tmem, a, (s2 >> 2) * 16384 + (s2 & 3) * 32, bst, (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32,
+                 idS, s2 > 0 ? 1u : 0u);
+        mma_commit(done);
       };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
         const int2 pr = p.q_pairs[item / p.hq];
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
-        if (!(ok = issue_sdp(it))) break;
+        if (!(ok = wait_kv(it))) break;
+        tc_fence_after();
+        issue_s(it, t_s, dq, dk, &bar_s_full);
+        issue_s(it, t_dp, ddo, dv, &bar_dp_full);
         for (int j = 0; j < n; ++j) {
           const int cur = it + j;
-          if (NS >= 2 && j + 1 < n && !(ok = issue_sdp(cur + 1))) break;
-          if (!(ok = mbar_wait(&bar_ds_ready[cur & 1], (cur >> 1) & 1, status))) break;
+          const bool more = j + 1 < n;
+          if (NS >= 2 && more) {
+            if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
+            if (!(ok = wait_kv(cur + 1))) break;
+            tc_fence_after();
+            issue_s(cur + 1, t_s, dq, dk, &bar_s_full);
+          }
+          if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
-          const int st = cur % NS;
-          const SmemDesc kst{dk_mn.lo + ((st * S::kKVBytes) >> 4), dk_mn.hi};
-          const uint32_t buf = tmem + S::kColBuf + (cur & 1) * 128;
+          const SmemDesc kst{dk_mn.lo + ((cur % NS) * S::kKVBytes >> 4), dk_mn.hi};
           const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-          for (int s2 = 0; s2 < kBN / 16; ++s2) {
-            const uint32_t acol = s2 * kGroupCols;  // 16 key rows packed by column group s2
-            mma_ts(t_dq, buf + acol, kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
+          for (int s2 = 0; s2 < kBN / 16; ++s2)
+            mma_ts(t_dq, t_dp + packed_col<kBN>(s2), kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
+          mma_commit(&bar_kv_empty[cur % NS]);
+          if (more) {
+            if (NS == 1) {
+              if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
+              if (!(ok = wait_kv(cur + 1))) break;
+              tc_fence_after();
+              issue_s(cur + 1, t_s, dq, dk, &bar_s_full);
+            }
+            issue_s(cur + 1, t_dp, ddo, dv, &bar_dp_full);
           }
-          mma_commit(&bar_kv_empty[st]);
-          if (NS == 1 && j + 1 < n && !(ok = issue_sdp(cur + 1))) break;
         }
         if (!ok) break;
         it += n;
@@ -584,7 +627,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int col0 = grp * kGroupCols;
+    const int col0 = grp * kG;
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
@@ -601,39 +644,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float dlt = row_valid ? p.delta_t[ti] : 0.f;
       const int lim = row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
       for (int j = 0; j < n; ++j, ++it) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[it & 1], (it >> 1) & 1, status));
+        const int nvalid = lim - (j * kBN + col0);
+        // ---- phase A: P = exp2(S * scale * log2e - lse2) into registers, then free S
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t buf = tmem + S::kColBuf + (it & 1) * 128 + lane_base + col0;
-        uint32_t sv[16], dv[16];
-        tmem_ld16(buf, sv);
-        tmem_ld16(buf + 64, dv);
-        tmem_ld_wait();
-        const int nvalid = lim - (j * kBN + col0);
-        uint32_t dd[8];
-        if (nvalid >= kGroupCols) {
+        float pv[kG];
+        {
+          uint32_t sv[kG];
+          if constexpr (kG == 32) tmem_ld32(tmem + S::kColS + lane_base + col0, sv);
+          else tmem_ld16(tmem + S::kColS + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(sv));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bar_s_free);
+          if (__all_sync(0xffffffffu, nvalid >= kG)) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float p0 = ex2b(fmaf(__uint_as_float(sv[2 * k]), sl2, -lse2));
-            const float p1 = ex2b(fmaf(__uint_as_float(sv[2 * k + 1]), sl2, -lse2));
-            dd[k] = pack2<kBF16>(p0 * (__uint_as_float(dv[2 * k]) - dlt),
-                                 p1 * (__uint_as_float(dv[2 * k + 1]) - dlt));
-          }
-        } else {
+            for (int i = 0; i < kG; ++i) pv[i] = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
+          } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int i0 = 2 * k, i1 = i0 + 1;
-            const float p0 = i0 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i0]), sl2, -lse2)) : 0.f;
-            const float p1 = i1 < nvalid ? ex2b(fmaf(__uint_as_float(sv[i1]), sl2, -lse2)) : 0.f;
-            const float d0 = i0 < nvalid ? p0 * (__uint_as_float(dv[i0]) - dlt) : 0.f;
-            const float d1 = i1 < nvalid ? p1 * (__uint_as_float(dv[i1]) - dlt) : 0.f;
-            dd[k] = pack2<kBF16>(d0, d1);
+            for (int i = 0; i < kG; ++i) {
+              const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
+              pv[i] = i < nvalid ? x : 0.f;
+            }
           }
         }
-        tmem_st8(buf, dd);
+        // ---- phase B: dS = P (dP - D), written over this warp's half of dP
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_dp_full, it & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t dv[kG];
+          if constexpr (kG == 32) tmem_ld32(tmem + S::kColDP + lane_base + col0, dv);
+          else tmem_ld16(tmem + S::kColDP + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(dv));
+          tmem_ld_wait();
+          uint32_t dd[kG / 2];
+#pragma unroll
+          for (int k = 0; k < kG / 2; ++k)
+            dd[k] = pack2<kBF16>(pv[2 * k] * (__uint_as_float(dv[2 * k]) - dlt),
+                                 pv[2 * k + 1] * (__uint_as_float(dv[2 * k + 1]) - dlt));
+          if constexpr (kG == 32) tmem_st16(tmem + S::kColDP + lane_base + col0, dd);
+          else tmem_st8(tmem + S::kColDP + lane_base + col0, *reinterpret_cast<uint32_t(*)[8]>(dd));
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_ds_ready[it & 1]);
+        mbar_arrive(&bar_ds_ready);
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
