@@ -220,10 +220,23 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld32(t_s + lane_base + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
         tmem_ld_wait();
         const int nvalid = min(max(lim - j * kBlockN, 0), kBlockN);
-        float mx = -INFINITY;
+        // Warp-uniform: only tiles on the causal diagonal or a length boundary pay
+        // for per-element masking. Max and sum use 8 independent partials so the
+        // dependent chains stay short.
+        const bool full = __all_sync(0xffffffffu, nvalid >= kBlockN);
+        float mp[8];
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c)
-          if (c < nvalid) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sr[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            mp[c & 7] = fmaxf(mp[c & 7], c < nvalid ? __uint_as_float(sr[c]) : -INFINITY);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
         const float mxs = mx * sl2;
         float m_new = m;
         bool rescale = false;
@@ -235,16 +248,30 @@ __global__ void __launch_bounds__(192, 1)
             rescale = true;
           }
         }
-        float rs = 0.f;
-        uint32_t pk[64];
+        float sp[8];
 #pragma unroll
-        for (int c = 0; c < kBlockN / 2; ++c) {
-          const float p0 = (2 * c < nvalid) ? ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_new)) : 0.f;
-          const float p1 =
-              (2 * c + 1 < nvalid) ? ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_new)) : 0.f;
-          rs += p0 + p1;
-          pk[c] = pack2<kBF16>(p0, p1);
+        for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+        uint32_t pk[64];
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kBlockN / 2; ++c) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_new));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_new));
+            sp[c & 7] += p0 + p1;
+            pk[c] = pack2<kBF16>(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBlockN / 2; ++c) {
+            const float x0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_new));
+            const float x1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_new));
+            const float p0 = 2 * c < nvalid ? x0 : 0.f;
+            const float p1 = 2 * c + 1 < nvalid ? x1 : 0.f;
+            sp[c & 7] += p0 + p1;
+            pk[c] = pack2<kBF16>(p0, p1);
+          }
         }
+        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         if (__any_sync(0xffffffffu, rescale)) {
           const int prev = cur - 1;
           ok = __all_sync(0xffffffffu,
