@@ -132,6 +132,26 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
  */
 int te_attn_read_status(const void* workspace, int* status, void* stream);
 
+/*
+ * Kernel timing (profiling aid). te_attn_profile_enable(1) makes every later call
+ * bracket each of its kernel launches with a pair of CUDA events recorded on the
+ * call's stream; te_attn_profile_read() synchronises on those events, adds each
+ * kernel's elapsed time and launch count into total_ms[k] / launches[k] for
+ * k = TE_KERNEL_* (arrays of at least TE_NUM_KERNELS entries), and clears the
+ * record. Disabled by default; while enabled, each launch costs two event
+ * records. Returns TE_OK or TE_ERR_CUDA. The record is process-wide (guarded by a
+ * mutex): calls from several threads land in the same totals.
+ */
+#define TE_KERNEL_SCHEDULE 0
+#define TE_KERNEL_FWD 1
+#define TE_KERNEL_ZERO_FILL 2
+#define TE_KERNEL_DELTA 3
+#define TE_KERNEL_DKDV 4
+#define TE_KERNEL_DQ 5
+#define TE_NUM_KERNELS 6
+int te_attn_profile_enable(int enable);
+int te_attn_profile_read(double* total_ms, int* launches);
+
 /* Thread-local description of the last error returned on this thread. */
 const char* te_attn_last_error(void);
 
