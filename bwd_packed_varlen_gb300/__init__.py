@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     MASK_PADDING_CAUSAL,
     TeAttnError,
     bwd,
+    bwd_noalloc,
     fwd,
     fwd_workspace_size,
     KERNELS,

@@ -56,6 +56,8 @@ def library() -> ctypes.CDLL:
     L.te_attn_fwd_thd.argtypes = [vp] * 5 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_bwd_thd.restype = i32
     L.te_attn_bwd_thd.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_bwd_thd_noalloc.restype = i32
+    L.te_attn_bwd_thd_noalloc.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp]
     L.te_attn_read_status.restype = i32
     L.te_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     L.te_attn_last_error.restype = ctypes.c_char_p
@@ -201,3 +203,31 @@ def profile_read() -> dict:
     cnt = (ctypes.c_int * n)()
     _check(library().te_attn_profile_read(ms, cnt))
     return {KERNELS[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                cu_seqlens_kv_padded, attn_scale, mask_type="padding", max_seqlen_q=0,
+                max_seqlen_kv=0, dq=None, dk=None, dv=None, stream=None):
+    """``te_attn_bwd_thd_noalloc``: the backward pass with the library's built-in
+    scratch array instead of a workspace, for callers that cannot allocate device
+    memory (the outputs here are still allocated by torch when not supplied)."""
+    L = library()
+    _need_cuda(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+               cu_seqlens_kv_padded, dq, dk, dv)
+    _cu(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded)
+    if q.dtype not in _DTYPES or any(t.dtype != q.dtype for t in (k, v, out, dout)):
+        raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
+    Tq, hq, d = q.shape
+    Tk, hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    rc = L.te_attn_bwd_thd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
+        _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+        d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], ctypes.c_void_p(st))
+    _check(rc)
+    return dq, dk, dv

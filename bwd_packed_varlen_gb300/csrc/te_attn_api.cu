@@ -176,6 +176,11 @@ cudaError_t timed(int kernel, cudaStream_t st, F&& launch) {
 
 }  // namespace
 
+namespace teattn {
+// Lets other entry points of the library report through te_attn_last_error().
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace teattn
+
 extern "C" {
 
 int te_attn_version(void) { return 10000; }

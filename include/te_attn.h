@@ -152,6 +152,35 @@ int te_attn_read_status(const void* workspace, int* status, void* stream);
 int te_attn_profile_enable(int enable);
 int te_attn_profile_read(double* total_ms, int* launches);
 
+/*
+ * Backward pass for callers that cannot allocate device memory (no counterpart in
+ * the pages this library follows; it is an interface addition). Some callers have
+ * no way to get scratch memory for a call: plugin hosts and inference servers that
+ * own every device allocation and give an operator only its inputs and outputs,
+ * runtimes that forbid allocation after start-up, foreign-language callers without
+ * a CUDA allocator. This variant of te_attn_bwd_thd takes the same arguments minus
+ * the workspace and uses a scratch array of TE_NOALLOC_SCRATCH_BYTES compiled into
+ * the library (a __device__ array: every GPU that loads it keeps it until the
+ * process exits). It calls no cudaMalloc, cudaFree or other allocating routine.
+ * - The first call on a device looks up the array's device address with that
+ *   device current and caches it; make that first call before any stream capture.
+ * - All calls on a device share the one array and it keeps the last call's
+ *   contents; nothing in it needs to start at zero (each call rewrites what it
+ *   reads), but calls that overlap on the GPU race on it: order them (one stream,
+ *   or events).
+ * - Returns TE_ERR_WORKSPACE_TOO_SMALL (and a message naming the size needed) when
+ *   te_attn_bwd_workspace_size() of the problem exceeds the array; otherwise the
+ *   same results and errors as te_attn_bwd_thd.
+ */
+#define TE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int te_attn_bwd_thd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                            const int32_t* cu_seqlens_q_padded,
+                            const int32_t* cu_seqlens_kv_padded, int batch, int total_q,
+                            int total_kv, int max_seqlen_q, int max_seqlen_kv, int hq, int hkv,
+                            int d, float attn_scale, int mask_type, int dtype, void* stream);
+
 /* Thread-local description of the last error returned on this thread. */
 const char* te_attn_last_error(void);
 
