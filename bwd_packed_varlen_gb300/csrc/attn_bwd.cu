@@ -34,10 +34,10 @@
 #include "launch.h"
 #include "sm103_ptx.cuh"
 #include "tmap.h"
+#include "work_queue.cuh"
 
 namespace teattn {
 
-constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2b(float x) {
   float y;
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ uint64_t bar_kv_full, bar_kv_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_q_full[NS], bar_q_empty[NS];
   __shared__ uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready;
+  __shared__ WorkRing ring;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_dp_full, 1);
     mbar_init(&bar_p_ready, kBwdComputeThreads);
     mbar_init(&bar_ds_ready, kBwdComputeThreads);
+    ring_init(ring, 1 + kBwdComputeThreads);
     fence_barrier_init();
   }
   if (warp == kWarpMma) {
@@ -213,7 +215,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tmV);
       int it = 0, ii = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      int nxt = blockIdx.x;
+      for (; ok; ++ii) {
+        const int item = nxt < n_items ? nxt : -1;
+        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
+        nxt = next_item(p.header + kHdrNextDkdv);  // used at the next hand-over
+
         const Item I = decode(item);
         if (ii > 0 && !(ok = mbar_wait(&bar_kv_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * S::kKVBytes);
@@ -274,7 +281,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int s = 0; s < kBM / 16; ++s)
           mma_ts(d_tmem, a_tmem + packed_col<kBM>(s), bst, s * 2048, idAcc, s > 0 ? 1u : acc0);
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      for (; ok; ++ii) {
+        const int item = ring_get(ring, ii, status, &ok);
+        if (!ok || item < 0) break;
+
         const Item I = decode(item);
         if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
         const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
@@ -321,7 +331,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+    for (; ok; ++ii) {
+      const int item = ring_get_warp(ring, ii, status, &ok);
+      if (!ok || item < 0) break;
+
       const Item I = decode(item);
       const int kv_row = I.kt * kBlockN + quarter * 32 + lane;
       const bool kv_valid = kv_row < I.s.len_k;
@@ -495,6 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_acc_full, bar_acc_empty;
   __shared__ uint64_t bar_kv_full[NS], bar_kv_empty[NS];
   __shared__ uint64_t bar_s_full, bar_dp_full, bar_s_free, bar_ds_ready;
+  __shared__ WorkRing ring;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -515,6 +529,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_dp_full, 1);
     mbar_init(&bar_s_free, kBwdComputeThreads);
     mbar_init(&bar_ds_ready, kBwdComputeThreads);
+    ring_init(ring, 1 + kBwdComputeThreads);
     fence_barrier_init();
   }
   if (warp == kWarpMma) {
@@ -534,7 +549,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tmV);
       int it = 0, ii = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      int nxt = blockIdx.x;
+      for (; ok; ++ii) {
+        const int item = nxt < n_items ? nxt : -1;
+        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
+        nxt = next_item(p.header + kHdrNextDq);  // used at the next hand-over
+
         const int2 pr = p.q_pairs[item / p.hq];
         const int h = item % p.hq, g = h / p.group;
         const SeqInfo s = load_seq(p, pr.x);
@@ -581,7 +601,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  idS, s2 > 0 ? 1u : 0u);
         mma_commit(done);
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      for (; ok; ++ii) {
+        const int item = ring_get(ring, ii, status, &ok);
+        if (!ok || item < 0) break;
+
         const int2 pr = p.q_pairs[item / p.hq];
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
@@ -631,7 +654,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale_log2;
     int it = 0, ii = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+    for (; ok; ++ii) {
+      const int item = ring_get_warp(ring, ii, status, &ok);
+      if (!ok || item < 0) break;
+
       const int2 pr = p.q_pairs[item / p.hq];
       const int h = item % p.hq;
       const SeqInfo s = load_seq(p, pr.x);

@@ -17,6 +17,9 @@ enum HeaderWord : int {
   kHdrStatus = 0,    // TE_STATUS_* bits raised by this call's kernels
   kHdrNumQPairs = 1, // number of (sequence, query tile) pairs
   kHdrNumKPairs = 2, // number of (sequence, key tile) pairs
+  kHdrNextFwd = 3,   // work counters of the persistent kernels (zeroed per call)
+  kHdrNextDkdv = 4,
+  kHdrNextDq = 5,
   kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
 };
 

@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
     p.header[kHdrStatus] = status;
     p.header[kHdrNumQPairs] = nq;
     p.header[kHdrNumKPairs] = nk;
+    p.header[kHdrNextFwd] = 0;
+    p.header[kHdrNextDkdv] = 0;
+    p.header[kHdrNextDq] = 0;
   }
 }
 
