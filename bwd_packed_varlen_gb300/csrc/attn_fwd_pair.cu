@@ -1,0 +1,423 @@
+// Forward attention, two query tiles per work item (head_dim <= 128).
+//
+// One work item = (sequence b, query head h, query rows [256u, 256u+256)): tile A
+// holds the first 128 rows, tile B the next 128 (absent when the sequence ends
+// before it). Both tiles read the same key/value tiles, so each K/V tile is loaded
+// once for 256 query rows. Roles:
+//   warps 0-3  softmax of tile A (one thread per query row / TMEM lane),
+//   warps 4-7  softmax of tile B,
+//   warp 8     TMA producer (Q_A, Q_B once per item; K_j, V_j rings),
+//   warp 9     MMA issuer (lane 0).
+// TMEM: O_A [0, 128), O_B [128, 256), S_A [256, 384), S_B [384, 512). The issue
+// order is  S_A0, S_B0 | PV_A0, S_A1 | PV_B0, S_B1 | PV_A1, S_A2 | ...  so while one
+// softmax warpgroup turns S into P the tensor cores work on the other tile. Since
+// S_X(j+1) is issued after PV_X(j), its completion also means PV_X(j) finished: the
+// softmax may rescale O_X as soon as S_X(j+1) is ready. P_X(j) is written as 16-bit
+// values over S_X(j) and read from TMEM by PV_X(j). The running max is rescaled
+// lazily (only when it grows by more than 2^8); masks use the REAL lengths and are
+// applied only on tiles that need them.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "sm103_ptx.cuh"
+#include "tmap.h"
+#include "work_queue.cuh"
+
+namespace teattn {
+
+template <int kD>
+struct FwdPairShape {
+  static_assert(kD == 64 || kD == 128, "two-tile forward supports head_dim up to 128");
+  static constexpr int kChunks = kD / 64;
+  static constexpr int kTileBytes = kChunks * 16384;  // 128 rows x kD cols x 2 B
+  static constexpr int kStages = 2;                   // K and V rings
+  static constexpr int kSmemUsed = kTileBytes * (2 + 2 * kStages) + 1024;
+  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  // TMEM columns of O_x and S_x for tile x (0: A, 1: B)
+  __device__ static constexpr uint32_t col_o(int x) { return static_cast<uint32_t>(x) * 128u; }
+  __device__ static constexpr uint32_t col_s(int x) { return 256u + static_cast<uint32_t>(x) * 128u; }
+};
+
+constexpr int kFwdPairThreads = 320;
+constexpr int kFwdWarpProducer = 8, kFwdWarpMma = 9;
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Per-item geometry, identical in every role.
+struct FwdItem {
+  SeqInfo s;
+  int h, g, u;
+  int n[2];      // key tiles tile A / tile B visit (0: tile absent)
+  int nmax;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool causal) {
+  FwdItem I;
+  const int2 pr = p.f_pairs[item / p.hq];
+  I.h = item % p.hq;
+  I.g = I.h / p.group;
+  I.u = pr.y;
+  I.s = load_seq(p, pr.x);
+  const int ta = 2 * I.u, tb = 2 * I.u + 1;
+  I.n[0] = (visible_keys(I.s, ta, causal) + kBlockN - 1) / kBlockN;
+  I.n[1] = tb * kBlockM < I.s.len_q ? (visible_keys(I.s, tb, causal) + kBlockN - 1) / kBlockN : 0;
+  I.nmax = I.n[0] > I.n[1] ? I.n[0] : I.n[1];
+  return I;
+}
+
+template <int kD, bool kBF16>
+__global__ void __launch_bounds__(kFwdPairThreads, 1)
+    attn_fwd_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using S = FwdPairShape<kD>;
+  constexpr int NS = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                          // tile A then tile B
+  uint8_t* sK = sQ + 2 * S::kTileBytes;        // NS stages
+  uint8_t* sV = sK + NS * S::kTileBytes;       // NS stages
+
+  __shared__ uint64_t bar_q_full, bar_q_empty;
+  __shared__ uint64_t bar_k_full[NS], bar_k_empty[NS], bar_v_full[NS], bar_v_empty[NS];
+  __shared__ uint64_t bar_s_full[2], bar_p_ready[2], bar_o_full[2], bar_o_empty[2];
+  __shared__ WorkRing ring;
+  __shared__ uint32_t tmem_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* status = p.header + kHdrStatus;
+  const int n_items = p.header[kHdrNumFPairs] * p.hq;
+  const bool causal = p.causal != 0;
+
+  if (tid == 0) {
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bar_k_full[i], 1);
+      mbar_init(&bar_k_empty[i], 1);
+      mbar_init(&bar_v_full[i], 1);
+      mbar_init(&bar_v_empty[i], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s_full[x], 1);
+      mbar_init(&bar_p_ready[x], 128);
+      mbar_init(&bar_o_full[x], 1);
+      mbar_init(&bar_o_empty[x], 128);
+    }
+    ring_init(ring, 1 + 256);
+    fence_barrier_init();
+  }
+  if (warp == kFwdWarpMma) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kFwdWarpProducer) {
+    // ------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int it = 0, ii = 0;
+      bool ok = true;
+      int nxt = blockIdx.x;
+      for (; ok; ++ii) {
+        const int item = nxt < n_items ? nxt : -1;
+        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
+        nxt = next_item(p.header + kHdrNextFwd);  // used at the next hand-over
+        const FwdItem I = fwd_item(p, item, causal);
+        if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
+        const int ntiles = I.n[1] > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(&bar_q_full, ntiles * S::kTileBytes);
+        for (int x = 0; x < ntiles; ++x)
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_3d(sQ + x * S::kTileBytes + c * 16384, &tmQ, &bar_q_full, c * 64, I.h,
+                        I.s.off_q + (2 * I.u + x) * kBlockM);
+        for (int j = 0; j < I.nmax; ++j, ++it) {
+          const int st = it % NS;
+          if (it >= NS && !(ok = mbar_wait(&bar_k_empty[st], ((it / NS) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bar_k_full[st], S::kTileBytes);
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_3d(sK + st * S::kTileBytes + c * 16384, &tmK, &bar_k_full[st], c * 64, I.g,
+                        I.s.off_k + j * kBlockN);
+          if (it >= NS && !(ok = mbar_wait(&bar_v_empty[st], ((it / NS) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bar_v_full[st], S::kTileBytes);
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_3d(sV + st * S::kTileBytes + c * 16384, &tmV, &bar_v_full[st], c * 64, I.g,
+                        I.s.off_k + j * kBlockN);
+        }
+      }
+    }
+  } else if (warp == kFwdWarpMma) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBlockN);
+      constexpr uint32_t idPV = make_idesc_f16(kBF16, false, true, 128, kD);
+      // Q and K K-major; V as the N-major (d-contiguous) B of P V.
+      const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
+      const SmemDesc dk = smem_desc(smem_u32(sK), 16, 1024, kLayoutSW128);
+      const SmemDesc dv = smem_desc(smem_u32(sV), 16384, 1024, kLayoutSW128);
+      int it = 0;
+      int np[2] = {0, 0};  // P hand-overs consumed per tile
+      int no[2] = {0, 0};  // items in which the tile was present
+      bool ok = true;
+      // S_x = Q_x K^T for the key tile in ring stage st.
+      auto issue_s = [&](int x, int st) {
+        const SmemDesc qx{dq.lo + ((x * S::kTileBytes) >> 4), dq.hi};
+        const SmemDesc kst{dk.lo + ((st * S::kTileBytes) >> 4), dk.hi};
+#pragma unroll
+        for (int s = 0; s < kD / 16; ++s) {
+          const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+          mma_ss(tmem + S::col_s(x), qx, off, kst, off, idS, s > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s_full[x]);
+      };
+      for (int ii = 0; ok; ++ii) {
+        const int item = ring_get(ring, ii, status, &ok);
+        if (!ok || item < 0) break;
+        const FwdItem I = fwd_item(p, item, causal);
+        if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
+        if (!(ok = mbar_wait(&bar_k_full[it % NS], (it / NS) & 1, status))) break;
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (I.n[x] > 0) issue_s(x, it % NS);
+        mma_commit(&bar_k_empty[it % NS]);
+        if (I.nmax == 1) mma_commit(&bar_q_empty);
+        for (int j = 0; j < I.nmax && ok; ++j) {
+          const int cur = it + j, st = cur % NS;
+          bool v_ready = false, k_ready = false;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j >= I.n[x]) continue;
+            if (!(ok = mbar_wait(&bar_p_ready[x], np[x] & 1, status))) break;
+            ++np[x];
+            if (j == 0 && no[x] > 0 && !(ok = mbar_wait(&bar_o_empty[x], (no[x] - 1) & 1, status))) break;
+            if (!v_ready) {
+              if (!(ok = mbar_wait(&bar_v_full[st], (cur / NS) & 1, status))) break;
+              v_ready = true;
+            }
+            tc_fence_after();
+            const SmemDesc vst{dv.lo + ((st * S::kTileBytes) >> 4), dv.hi};
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+            for (int s = 0; s < kBlockN / 16; ++s)
+              mma_ts(tmem + S::col_o(x), tmem + S::col_s(x) + s * 8, vst, s * 2048, idPV,
+                     s > 0 ? 1u : acc0);
+            if (j + 1 < I.n[x]) {
+              const int nx = cur + 1;
+              if (!k_ready) {
+                if (!(ok = mbar_wait(&bar_k_full[nx % NS], (nx / NS) & 1, status))) break;
+                k_ready = true;
+              }
+              tc_fence_after();
+              issue_s(x, nx % NS);
+            } else {
+              mma_commit(&bar_o_full[x]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar_v_empty[st]);
+          if (j + 1 < I.nmax) mma_commit(&bar_k_empty[(cur + 1) % NS]);
+          if (j + 2 == I.nmax) mma_commit(&bar_q_empty);
+        }
+        if (!ok) break;
+        for (int x = 0; x < 2; ++x)
+          if (I.n[x] > 0) ++no[x];
+        it += I.nmax;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax A / B
+    const int x = warp >> 2;  // 0: tile A, 1: tile B
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + S::col_s(x) + lane_base;
+    const uint32_t t_o = tmem + S::col_o(x) + lane_base;
+    const float sl2 = p.scale_log2;
+    using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+    int ns = 0, no = 0;  // S hand-overs and items seen by this tile
+    bool ok = true;
+    for (int ii = 0; ok; ++ii) {
+      const int item = ring_get_warp(ring, ii, status, &ok);
+      if (!ok || item < 0) break;
+      const FwdItem I = fwd_item(p, item, causal);
+      const int n = I.n[x];
+      if (n == 0) continue;
+      const int row = (2 * I.u + x) * kBlockM + quarter * 32 + lane;
+      const bool row_valid = row < I.s.len_q;
+      const int lim = row_valid ? (causal ? min(I.s.len_k, row + 1) : I.s.len_k) : 0;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], ns & 1, status));
+        if (!ok) break;
+        ++ns;
+        tc_fence_after();
+        const int nvalid = min(max(lim - j * kBlockN, 0), kBlockN);
+        const bool full = __all_sync(0xffffffffu, nvalid >= kBlockN);
+        // pass 1: row max over the four 32-column chunks (8 independent partials)
+        float mp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
+          uint32_t sv[32];
+          tmem_ld32(t_s + c0, sv);
+          tmem_ld_wait();
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sv[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              mp[c & 7] = fmaxf(mp[c & 7], c0 + c < nvalid ? __uint_as_float(sv[c]) : -INFINITY);
+          }
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        const float mxs = mx * sl2;
+        float m_new = m;
+        bool rescale = false;
+        if (nvalid > 0) {
+          if (m == -INFINITY) {
+            m_new = mxs;
+          } else if (mxs > m + 8.0f) {
+            m_new = mxs;
+            rescale = true;
+          }
+        }
+        float alpha = 1.f;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_x is final for tiles < j: S_x(j) was issued after PV_x(j-1).
+          alpha = rescale ? ex2f(m - m_new) : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st16(t_o + c0, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+            tmem_st16(t_o + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+          }
+        }
+        // pass 2: P = exp2(S * scale * log2e - m), packed over the chunk's first
+        // half-width columns (chunk c writes [16c, 16c+16), already read)
+        float sp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
+          uint32_t sv[32], pk[16];
+          tmem_ld32(t_s + c0, sv);
+          tmem_ld_wait();
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_new));
+              const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_new));
+              sp[c & 7] += p0 + p1;
+              pk[c] = pack2<kBF16>(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float x0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_new));
+              const float x1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_new));
+              const float p0 = c0 + 2 * c < nvalid ? x0 : 0.f;
+              const float p1 = c0 + 2 * c + 1 < nvalid ? x1 : 0.f;
+              sp[c & 7] += p0 + p1;
+              pk[c] = pack2<kBF16>(p0, p1);
+            }
+          }
+          tmem_st16(t_s + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_p_ready[x]);
+        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        l = l * alpha + rs;
+        m = m_new;
+      }
+      if (!ok) break;
+      // epilogue: O / l and lse for this row once the tile's last P V has landed
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full[x], no & 1, status));
+      if (!ok) break;
+      ++no;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      T* orow = static_cast<T*>(p.out) +
+                (static_cast<size_t>(I.s.off_q + row) * p.hq + I.h) * static_cast<size_t>(p.d);
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c0, o);
+        tmem_ld_wait();
+        if (row_valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int col = c0 + v * 8;
+            if (col + 8 <= p.d) {
+              uint4 w;
+              w.x = pack2<kBF16>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
+              w.y = pack2<kBF16>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
+              w.z = pack2<kBF16>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
+              w.w = pack2<kBF16>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + col) = w;
+            }
+          }
+        }
+      }
+      if (row_valid)
+        p.lse[static_cast<size_t>(I.s.off_q + row) * p.hq + I.h] = m * 0.69314718055994531f + logf(l);
+      tc_fence_before();
+      mbar_arrive(&bar_o_empty[x]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kFwdWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int kD, bool kBF16>
+static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
+  using S = FwdPairShape<kD>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16) ||
+      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16) ||
+      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16))
+    return cudaErrorInvalidValue;
+  auto kern = attn_fwd_pair_kernel<kD, kBF16>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long max_items = static_cast<long long>(p.pair_cap_f) * p.hq;
+  const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
+  kern<<<grid, kFwdPairThreads, S::kSmemBytes, st>>>(p, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_pair(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st) {
+  if (bf16) return p.d <= 64 ? launch_fwd_pair_impl<64, true>(p, num_sms, st)
+                             : launch_fwd_pair_impl<128, true>(p, num_sms, st);
+  return p.d <= 64 ? launch_fwd_pair_impl<64, false>(p, num_sms, st)
+                   : launch_fwd_pair_impl<128, false>(p, num_sms, st);
+}
+
+}  // namespace teattn

@@ -11,6 +11,8 @@ namespace teattn {
 // MMA) by 128 key rows per step.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
+// The forward takes two consecutive query tiles of one sequence and head per item.
+constexpr int kBlockF = 2 * kBlockM;
 
 // Workspace header (int32 words at the start of every workspace).
 enum HeaderWord : int {
@@ -20,6 +22,7 @@ enum HeaderWord : int {
   kHdrNextFwd = 3,   // work counters of the persistent kernels (zeroed per call)
   kHdrNextDkdv = 4,
   kHdrNextDq = 5,
+  kHdrNumFPairs = 6, // number of (sequence, 256-row query tile pair) items
   kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
 };
 
@@ -64,8 +67,10 @@ struct AttnParams {
   int* header;       // workspace header (status, pair counts)
   int2* q_pairs;     // sorted (sequence, query tile) pairs
   int2* k_pairs;     // sorted (sequence, key tile) pairs
+  int2* f_pairs;     // sorted (sequence, 256-row query tile) pairs (forward)
   int pair_cap_q;    // capacity of q_pairs
   int pair_cap_k;    // capacity of k_pairs
+  int pair_cap_f;    // capacity of f_pairs
 };
 
 // Real length and padded offset of sequence b, validated against the tensor

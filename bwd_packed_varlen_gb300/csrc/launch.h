@@ -8,11 +8,13 @@
 
 namespace teattn {
 
-cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, cudaStream_t st);
+cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, int* pref_f,
+                            cudaStream_t st);
 cudaError_t launch_zero_fill(const AttnParams& p, int mode, int num_sms, cudaStream_t st);
 cudaError_t launch_delta(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 
 cudaError_t launch_attn_fwd(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_attn_fwd_pair(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 

@@ -14,9 +14,10 @@ namespace teattn {
 // ---------------------------------------------------------------------------
 // Scheduler
 // ---------------------------------------------------------------------------
-// One 1024-thread block turns the four cu_seqlens arrays into two lists:
-//   q pairs  (sequence, query tile)  -- forward and dQ items (x hq heads)
-//   k pairs  (sequence, key tile)    -- dK/dV items (x hkv heads)
+// One 1024-thread block turns the four cu_seqlens arrays into three lists:
+//   q pairs  (sequence, query tile)            -- dQ items (x hq heads)
+//   k pairs  (sequence, key tile)              -- dK/dV items (x hkv heads)
+//   f pairs  (sequence, pair of query tiles)   -- forward items (x hq heads)
 // Tiles cover the REAL length of each sequence; sequences without a real query
 // or key produce no pair, and key tiles no real query sees (causal, beyond the
 // query length) produce none either -- those rows are zero-filled instead.
@@ -74,7 +75,18 @@ __device__ int k_pair_cost(const AttnParams& p, int b, int t) {
   return p.causal ? nq - (t * kBlockN) / kBlockM : nq;
 }
 
-template <bool kIsQ>
+// Forward item of two query tiles: both tiles' key tiles (the second sees most).
+__device__ int f_pair_cost(const AttnParams& p, int b, int t) {
+  SeqInfo s = load_seq(p, b);
+  const int a = (visible_keys(s, 2 * t, p.causal) + kBlockN - 1) / kBlockN;
+  const int c = 2 * t * kBlockM + kBlockM < s.len_q
+                    ? (visible_keys(s, 2 * t + 1, p.causal) + kBlockN - 1) / kBlockN
+                    : 0;
+  return a + c;
+}
+
+// kKind: 0 query tiles, 1 key tiles, 2 forward pairs of query tiles.
+template <int kKind>
 __device__ void build_list(const AttnParams& p, const int* pref, int n, int2* out,
                            uint64_t* keys) {
   const int B = p.batch;
@@ -86,7 +98,8 @@ __device__ void build_list(const AttnParams& p, const int* pref, int n, int2* ou
       if (i < n) {
         int b = find_seq(pref, B, i);
         int t = i - pref[b];
-        int cost = kIsQ ? q_pair_cost(p, b, t) : k_pair_cost(p, b, t);
+        int cost = kKind == 0 ? q_pair_cost(p, b, t)
+                   : (kKind == 1 ? k_pair_cost(p, b, t) : f_pair_cost(p, b, t));
         key = (static_cast<uint64_t>(0x7fffffffu - static_cast<uint32_t>(cost)) << 32) |
               static_cast<uint32_t>(i);
       }
@@ -124,63 +137,73 @@ __device__ void build_list(const AttnParams& p, const int* pref, int n, int2* ou
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, int* pref_q,
-                                                                  int* pref_k) {
+                                                                  int* pref_k, int* pref_f) {
   extern __shared__ uint64_t sort_keys[];
   __shared__ int warp_sums[32];
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
-  int carry_q = 0, carry_k = 0;
+  int carry_q = 0, carry_k = 0, carry_f = 0;
   for (int base = 0; base < p.batch; base += blockDim.x) {
     int b = base + threadIdx.x;
-    int cq = 0, ck = 0;
+    int cq = 0, ck = 0, cf = 0;
     if (b < p.batch) {
       SeqInfo s = load_seq(p, b);
       if (!s.ok) bad = 1;
       if (s.len_q > 0 && s.len_k > 0) {
         cq = (s.len_q + kBlockM - 1) / kBlockM;
         ck = (seen_keys(s, p.causal) + kBlockN - 1) / kBlockN;
+        cf = (s.len_q + kBlockF - 1) / kBlockF;
       }
     }
-    int tq, tk;
+    int tq, tk, tf;
     int eq = block_excl_scan(cq, warp_sums, &tq);
     int ek = block_excl_scan(ck, warp_sums, &tk);
+    int ef = block_excl_scan(cf, warp_sums, &tf);
     if (b < p.batch) {
       pref_q[b] = carry_q + eq;
       pref_k[b] = carry_k + ek;
+      pref_f[b] = carry_f + ef;
     }
     carry_q += tq;
     carry_k += tk;
+    carry_f += tf;
   }
   if (threadIdx.x == 0) {
     pref_q[p.batch] = carry_q;
     pref_k[p.batch] = carry_k;
+    pref_f[p.batch] = carry_f;
   }
   __threadfence_block();
   __syncthreads();
   const int nq = min(carry_q, p.pair_cap_q);
   const int nk = min(carry_k, p.pair_cap_k);
-  build_list<true>(p, pref_q, nq, p.q_pairs, sort_keys);
-  build_list<false>(p, pref_k, nk, p.k_pairs, sort_keys);
+  const int nf = min(carry_f, p.pair_cap_f);
+  build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
+  build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
+  build_list<2>(p, pref_f, nf, p.f_pairs, sort_keys);
   if (threadIdx.x == 0) {
     int status = bad ? kStatusBadSeqlens : 0;
-    if (carry_q > p.pair_cap_q || carry_k > p.pair_cap_k) status |= kStatusBadSeqlens;
+    if (carry_q > p.pair_cap_q || carry_k > p.pair_cap_k || carry_f > p.pair_cap_f)
+      status |= kStatusBadSeqlens;
     p.header[kHdrStatus] = status;
     p.header[kHdrNumQPairs] = nq;
     p.header[kHdrNumKPairs] = nk;
+    p.header[kHdrNumFPairs] = nf;
     p.header[kHdrNextFwd] = 0;
     p.header[kHdrNextDkdv] = 0;
     p.header[kHdrNextDq] = 0;
   }
 }
 
-cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, cudaStream_t st) {
+cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, int* pref_f,
+                            cudaStream_t st) {
   const size_t smem = kSortCap * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, st>>>(p, pref_q, pref_k);
+  schedule_kernel<<<1, kSchedThreads, smem, st>>>(p, pref_q, pref_k, pref_f);
   return cudaGetLastError();
 }
 

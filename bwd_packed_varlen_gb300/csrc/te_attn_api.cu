@@ -36,16 +36,18 @@ int ok_status() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t header, pref_q, pref_k, q_pairs, k_pairs, lse_t, delta_t, total;
-  int cap_q, cap_k;
+  size_t header, pref_q, pref_k, pref_f, q_pairs, k_pairs, f_pairs, lse_t, delta_t, total;
+  int cap_q, cap_k, cap_f;
 };
 
 // Workspace layout (256-byte aligned sections):
 //   header  int32[64]        status word and pair counts of this call
 //   pref_q  int32[batch+1]   prefix sums of query tiles per sequence
 //   pref_k  int32[batch+1]   prefix sums of key tiles per sequence
+//   pref_f  int32[batch+1]   prefix sums of 256-row query tile pairs per sequence
 //   q_pairs int2[cap_q]      sorted (sequence, query tile)
 //   k_pairs int2[cap_k]      sorted (sequence, key tile)
+//   f_pairs int2[cap_f]      sorted (sequence, 256-row query tile pair)
 //   lse_t   fp32[cap_q*hq*128] backward only: lse * log2(e), tile-major
 //   delta_t fp32[cap_q*hq*128] backward only: rowsum(dO * O), tile-major
 bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L) {
@@ -53,9 +55,11 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
   const long long cq = static_cast<long long>(total_q) / teattn::kBlockM + batch + 1;
   const long long ck = static_cast<long long>(total_kv) / teattn::kBlockN + batch + 1;
+  const long long cf = static_cast<long long>(total_q) / teattn::kBlockF + batch + 1;
   if (cq > INT32_MAX / 64 || ck > INT32_MAX / 64) return false;
   L->cap_q = static_cast<int>(cq);
   L->cap_k = static_cast<int>(ck);
+  L->cap_f = static_cast<int>(cf);
   size_t off = 0;
   L->header = off;
   off = align_up(off + teattn::kHdrWords * sizeof(int), 256);
@@ -63,10 +67,14 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   off = align_up(off + (static_cast<size_t>(batch) + 1) * sizeof(int), 256);
   L->pref_k = off;
   off = align_up(off + (static_cast<size_t>(batch) + 1) * sizeof(int), 256);
+  L->pref_f = off;
+  off = align_up(off + (static_cast<size_t>(batch) + 1) * sizeof(int), 256);
   L->q_pairs = off;
   off = align_up(off + static_cast<size_t>(cq) * sizeof(int2), 256);
   L->k_pairs = off;
   off = align_up(off + static_cast<size_t>(ck) * sizeof(int2), 256);
+  L->f_pairs = off;
+  off = align_up(off + static_cast<size_t>(cf) * sizeof(int2), 256);
   const size_t tiled = static_cast<size_t>(cq) * hq * teattn::kBlockM * sizeof(float);
   L->lse_t = off;
   if (backward) off = align_up(off + tiled, 256);
@@ -138,8 +146,10 @@ teattn::AttnParams base_params(const int32_t* cu_q, const int32_t* cu_kv, const 
   p.header = reinterpret_cast<int*>(ws + L.header);
   p.q_pairs = reinterpret_cast<int2*>(ws + L.q_pairs);
   p.k_pairs = reinterpret_cast<int2*>(ws + L.k_pairs);
+  p.f_pairs = reinterpret_cast<int2*>(ws + L.f_pairs);
   p.pair_cap_q = L.cap_q;
   p.pair_cap_k = L.cap_k;
+  p.pair_cap_f = L.cap_f;
   return p;
 }
 
@@ -236,10 +246,13 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
   const bool bf16 = dtype == TE_DTYPE_BF16;
-  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, st); });
+  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, reinterpret_cast<int*>(ws + L.pref_f), st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   if (total_q > 0 && total_kv > 0) {
-    e = timed(TE_KERNEL_FWD, st, [&] { return teattn::launch_attn_fwd(p, bf16, sms, st); });
+    e = timed(TE_KERNEL_FWD, st, [&] {
+      return d <= 128 ? teattn::launch_attn_fwd_pair(p, bf16, sms, st)
+                      : teattn::launch_attn_fwd(p, bf16, sms, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "attention forward");
   }
   if (total_q > 0) {
@@ -295,7 +308,7 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
   p.pref_q = pref_q;
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
   const bool bf16 = dtype == TE_DTYPE_BF16;
-  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, st); });
+  cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, reinterpret_cast<int*>(ws + L.pref_f), st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   if (total_q > 0) {
     e = timed(TE_KERNEL_DELTA, st, [&] { return teattn::launch_delta(p, bf16, sms, st); });
