@@ -266,10 +266,10 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         tc_fence_after();
         const int nvalid = min(max(lim - j * kBlockN, 0), kBlockN);
         const bool full = __all_sync(0xffffffffu, nvalid >= kBlockN);
-        // pass 1: row max over the four 32-column chunks (8 independent partials)
-        float mp[8];
+        // pass 1: row max over the four 32-column chunks (4 independent 3-input chains)
+        float mp[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+        for (int k = 0; k < 4; ++k) mp[k] = -INFINITY;
 #pragma unroll
         for (int c0 = 0; c0 < kBlockN; c0 += 32) {
           uint32_t sv[32];
@@ -277,15 +277,16 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
           tmem_ld_wait();
           if (full) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(sv[c]));
+            for (int c = 0; c < 32; c += 2)
+              mp[(c >> 1) & 3] = max3(mp[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              mp[c & 7] = fmaxf(mp[c & 7], c0 + c < nvalid ? __uint_as_float(sv[c]) : -INFINITY);
+            for (int c = 0; c < 32; c += 2)
+              mp[(c >> 1) & 3] = max3(mp[(c >> 1) & 3], c0 + c < nvalid ? __uint_as_float(sv[c]) : -INFINITY,
+                                      c0 + c + 1 < nvalid ? __uint_as_float(sv[c + 1]) : -INFINITY);
           }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        const float mx = fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]);
         const float mxs = mx * sl2;
         float m_new = m;
         bool rescale = false;
@@ -314,39 +315,35 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         }
         // pass 2: P = exp2(S * scale * log2e - m), packed over the chunk's first
         // half-width columns (chunk c writes [16c, 16c+16), already read)
-        float sp[8];
+        // x = s * scale*log2e - m on pairs; sums accumulate in 4 paired partials
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_new, -m_new);
+        uint64_t sp[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+        for (int k = 0; k < 4; ++k) sp[k] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c0 = 0; c0 < kBlockN; c0 += 32) {
           uint32_t sv[32], pk[16];
           tmem_ld32(t_s + c0, sv);
           tmem_ld_wait();
-          if (full) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_new));
-              const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_new));
-              sp[c & 7] += p0 + p1;
-              pk[c] = pack2<kBF16>(p0, p1);
+          for (int c = 0; c < 16; ++c) {
+            const float2 xx = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])),
+                                              sl2x2, negm2));
+            float p0 = ex2f(xx.x), p1 = ex2f(xx.y);
+            if (!full) {
+              p0 = c0 + 2 * c < nvalid ? p0 : 0.f;
+              p1 = c0 + 2 * c + 1 < nvalid ? p1 : 0.f;
             }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float x0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_new));
-              const float x1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_new));
-              const float p0 = c0 + 2 * c < nvalid ? x0 : 0.f;
-              const float p1 = c0 + 2 * c + 1 < nvalid ? x1 : 0.f;
-              sp[c & 7] += p0 + p1;
-              pk[c] = pack2<kBF16>(p0, p1);
-            }
+            sp[c & 3] = fadd2(sp[c & 3], f2_pack(p0, p1));
+            pk[c] = pack2<kBF16>(p0, p1);
           }
           tmem_st16(t_s + c0 / 2, pk);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_p_ready[x]);
-        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        const float2 s01 = f2_unpack(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
+        const float rs = s01.x + s01.y;
         l = l * alpha + rs;
         m = m_new;
       }

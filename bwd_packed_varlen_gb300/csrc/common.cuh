@@ -26,6 +26,9 @@ enum HeaderWord : int {
   kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
 };
 
+// Work lists the scheduler sorts for a call (the prefix sums are always built).
+constexpr int kListQ = 1, kListK = 2, kListF = 4;
+
 constexpr int kStatusBadSeqlens = 1;
 constexpr int kStatusTimeout = 2;
 
@@ -71,6 +74,7 @@ struct AttnParams {
   int pair_cap_q;    // capacity of q_pairs
   int pair_cap_k;    // capacity of k_pairs
   int pair_cap_f;    // capacity of f_pairs
+  int sched_lists;   // kList* bits: lists this call's kernels read
 };
 
 // Real length and padded offset of sequence b, validated against the tensor

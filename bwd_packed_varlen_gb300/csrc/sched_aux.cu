@@ -179,9 +179,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
   const int nq = min(carry_q, p.pair_cap_q);
   const int nk = min(carry_k, p.pair_cap_k);
   const int nf = min(carry_f, p.pair_cap_f);
-  build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
-  build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
-  build_list<2>(p, pref_f, nf, p.f_pairs, sort_keys);
+  if (p.sched_lists & kListQ) build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
+  if (p.sched_lists & kListK) build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
+  if (p.sched_lists & kListF) build_list<2>(p, pref_f, nf, p.f_pairs, sort_keys);
   if (threadIdx.x == 0) {
     int status = bad ? kStatusBadSeqlens : 0;
     if (carry_q > p.pair_cap_q || carry_k > p.pair_cap_k || carry_f > p.pair_cap_f)
@@ -321,12 +321,25 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
     const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) +
                                                     row * p.hq * p.d);
     if (32 % cpr == 0) {
-      for (int c0 = 0; c0 < chunks; c0 += 32) {
-        int c = c0 + lane;
-        float v = c < chunks ? dot8<T>(o[c], g[c]) : 0.f;
-        for (int w = cpr >> 1; w > 0; w >>= 1) v += __shfl_xor_sync(0xffffffffu, v, w);
-        if (c < chunks && (c % cpr) == 0)
-          p.delta_t[t0 + static_cast<size_t>(c / cpr) * kBlockM] = v;
+      // Four 32-chunk groups per pass: all loads of a pass are in flight together.
+      for (int c0 = 0; c0 < chunks; c0 += 128) {
+        uint4 oa[4], ga[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u + lane;
+          if (c < chunks) {
+            oa[u] = o[c];
+            ga[u] = g[c];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u + lane;
+          float v = c < chunks ? dot8<T>(oa[u], ga[u]) : 0.f;
+          for (int w = cpr >> 1; w > 0; w >>= 1) v += __shfl_xor_sync(0xffffffffu, v, w);
+          if (c < chunks && (c % cpr) == 0)
+            p.delta_t[t0 + static_cast<size_t>(c / cpr) * kBlockM] = v;
+        }
       }
     } else {
       for (int h = lane; h < p.hq; h += 32) {

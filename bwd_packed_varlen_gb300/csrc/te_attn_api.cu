@@ -242,6 +242,7 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   p.v = v;
   p.out = out;
   p.lse = lse;
+  p.sched_lists = d <= 128 ? teattn::kListF : teattn::kListQ;
   char* ws = static_cast<char*>(workspace);
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
@@ -295,6 +296,7 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
   p.q = q;
   p.k = k;
   p.v = v;
+  p.sched_lists = teattn::kListQ | teattn::kListK;
   p.out_in = out;
   p.dout = dout;
   p.lse_in = lse;
