@@ -37,7 +37,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -74,7 +74,9 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms by a reader thread that stamps each line on
+    arrival; only samples taken between ``mark_start()`` and ``mark_end()`` (the
+    timed region) are summarised."""
 
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -83,27 +85,52 @@ class ClockSampler:
     def __init__(self, uuid):
         self.uuid = uuid
         self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line))
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                bufsize=1)
         except Exception:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
         self.proc.terminate()
         try:
-            text, _ = self.proc.communicate(timeout=10)
+            self.proc.wait(timeout=10)
         except Exception:
             self.proc.kill()
-            text = ""
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = self.t1 if self.t1 is not None else math.inf
         sm, smax, pw, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in text.splitlines():
+        for stamp, line in list(self.lines):
+            # a line arrives at most one sampling period after it was taken
+            if not (t0 < stamp <= t1 + 0.1):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -119,9 +146,9 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm),
+                "sm_min_mhz": min(sm), "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_median": statistics.median(pw)}
 
 
@@ -295,12 +322,14 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    clocks.mark_start()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record()
         step(t["q"], t["k"], t["v"], t["dout"], cu)
         ends[i].record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     barrier()
     clk = clocks.stop()
     ta.profile_enable(False)

@@ -475,6 +475,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // dP at kColS + 128. The MMA thread issues  S_j, dP_j, | S_j+1, dQ_j, dP_j+1 | ...:
 // S_j+1 goes out as soon as the compute warps have read S_j into registers, dQ_j
 // once they have written dS_j (over their half of dP_j), dP_j+1 after dQ_j.
+// K and V stream through separate rings: a K tile is read until dQ_j, late in
+// step j, and S_j+1 wants the next one early, so the K ring is the deeper one;
+// a V tile is free as soon as dP_j has read it.
 template <int kD>
 struct DqShape {
   static constexpr int kBN = kD <= 128 ? 128 : 64;     // key rows per step
@@ -482,12 +485,14 @@ struct DqShape {
   static constexpr int kQBytes = kChunks * 16384;      // 128-row Q or dO tile
   static constexpr int kKVBytes = kChunks * kBN * 128; // kBN-row K or V tile
   static constexpr int kFixed = 2 * kQBytes + 1024 + 2048;
-  static constexpr int kStages = cmin(4, (227 * 1024 - kFixed) / (2 * kKVBytes));
-  static constexpr int kSmemUsed = 2 * kQBytes + kStages * 2 * kKVBytes + 1024;
+  static constexpr int kTiles = cmin(8, (227 * 1024 - kFixed) / kKVBytes);  // K + V stages
+  static constexpr int kKStages = cmin(4, (kTiles + 1) / 2);
+  static constexpr int kVStages = cmin(4, kTiles - kKStages);
+  static constexpr int kSmemUsed = 2 * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
   static constexpr int kG = kBN / kColGroups;          // key columns per compute warp
   static constexpr uint32_t kColDQ = 0, kColS = kD <= 128 ? 128 : 256, kColDP = kColS + 128;
-  static_assert(kStages >= 1, "shared memory budget");
+  static_assert(kKStages >= 2 && kVStages >= 1, "shared memory budget");
 };
 
 template <int kD, bool kBF16>
@@ -496,17 +501,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
   using S = DqShape<kD>;
-  constexpr int kBN = S::kBN, NS = S::kStages, kG = S::kG;
+  constexpr int kBN = S::kBN, KS = S::kKStages, VS = S::kVStages, kG = S::kG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + S::kQBytes;
-  uint8_t* sK = sDO + S::kQBytes;          // NS stages
-  uint8_t* sV = sK + NS * S::kKVBytes;     // NS stages
+  uint8_t* sK = sDO + S::kQBytes;          // KS stages
+  uint8_t* sV = sK + KS * S::kKVBytes;     // VS stages
 
   __shared__ uint64_t bar_q_full, bar_q_empty, bar_acc_full, bar_acc_empty;
-  __shared__ uint64_t bar_kv_full[NS], bar_kv_empty[NS];
+  __shared__ uint64_t bar_k_full[KS], bar_k_empty[KS], bar_v_full[VS], bar_v_empty[VS];
   __shared__ uint64_t bar_s_full, bar_dp_full, bar_s_free, bar_ds_ready;
   __shared__ WorkRing ring;
   __shared__ uint32_t tmem_slot;
@@ -521,9 +526,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_acc_full, 1);
     mbar_init(&bar_acc_empty, kBwdComputeThreads);
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&bar_kv_full[i], 1);
-      mbar_init(&bar_kv_empty[i], 1);
+    for (int i = 0; i < KS; ++i) {
+      mbar_init(&bar_k_full[i], 1);
+      mbar_init(&bar_k_empty[i], 1);
+    }
+    for (int i = 0; i < VS; ++i) {
+      mbar_init(&bar_v_full[i], 1);
+      mbar_init(&bar_v_empty[i], 1);
     }
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_dp_full, 1);
@@ -566,15 +575,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sDO + c * 16384, &tmDO, &bar_q_full, c * 64, h, s.off_q + pr.y * kBlockM);
         }
         for (int j = 0; j < n; ++j, ++it) {
-          const int st = it % NS;
-          if (it >= NS && !(ok = mbar_wait(&bar_kv_empty[st], ((it / NS) - 1) & 1, status))) break;
-          mbar_arrive_expect_tx(&bar_kv_full[st], 2 * S::kKVBytes);
-          for (int c = 0; c < S::kChunks; ++c) {
-            tma_load_3d(sK + st * S::kKVBytes + c * kBN * 128, &tmK, &bar_kv_full[st], c * 64, g,
+          const int sk = it % KS, sv = it % VS;
+          if (it >= KS && !(ok = mbar_wait(&bar_k_empty[sk], ((it / KS) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bar_k_full[sk], S::kKVBytes);
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_3d(sK + sk * S::kKVBytes + c * kBN * 128, &tmK, &bar_k_full[sk], c * 64, g,
                         s.off_k + j * kBN);
-            tma_load_3d(sV + st * S::kKVBytes + c * kBN * 128, &tmV, &bar_kv_full[st], c * 64, g,
+          if (it >= VS && !(ok = mbar_wait(&bar_v_empty[sv], ((it / VS) - 1) & 1, status))) break;
+          mbar_arrive_expect_tx(&bar_v_full[sv], S::kKVBytes);
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_3d(sV + sv * S::kKVBytes + c * kBN * 128, &tmV, &bar_v_full[sv], c * 64, g,
                         s.off_k + j * kBN);
-          }
         }
       }
     }
@@ -591,10 +602,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SmemDesc dk_mn = smem_desc(smem_u32(sK), kBN * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      auto wait_kv = [&](int cur) { return mbar_wait(&bar_kv_full[cur % NS], (cur / NS) & 1, status); };
-      // S = Q K^T (a = Q, b = K stage) or dP = dO V^T (a = dO, b = V stage) for step `cur`.
-      auto issue_s = [&](int cur, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
-        const SmemDesc bst{b.lo + ((cur % NS) * S::kKVBytes >> 4), b.hi};
+      auto wait_k = [&](int cur) { return mbar_wait(&bar_k_full[cur % KS], (cur / KS) & 1, status); };
+      auto wait_v = [&](int cur) { return mbar_wait(&bar_v_full[cur % VS], (cur / VS) & 1, status); };
+      // S = Q K^T (a = Q, b = K stage) or dP = dO V^T (a = dO, b = V stage).
+      auto issue_s = [&](int stage, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
+        const SmemDesc bst{b.lo + (stage * S::kKVBytes >> 4), b.hi};
 #pragma unroll
         for (int s2 = 0; s2 < kD / 16; ++s2)
           mma_ss(d_tmem, a, (s2 >> 2) * 16384 + (s2 & 3) * 32, bst, (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32,
@@ -609,36 +621,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
-        if (!(ok = wait_kv(it))) break;
+        if (!(ok = wait_k(it))) break;
         tc_fence_after();
-        issue_s(it, t_s, dq, dk, &bar_s_full);
-        issue_s(it, t_dp, ddo, dv, &bar_dp_full);
+        issue_s(it % KS, t_s, dq, dk, &bar_s_full);
+        if (!(ok = wait_v(it))) break;
+        tc_fence_after();
+        issue_s(it % VS, t_dp, ddo, dv, &bar_dp_full);
+        mma_commit(&bar_v_empty[it % VS]);
         for (int j = 0; j < n; ++j) {
           const int cur = it + j;
           const bool more = j + 1 < n;
-          if (NS >= 2 && more) {
+          if (more) {  // S_j+1 into the S buffer once S_j has been read (KS >= 2)
             if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
-            if (!(ok = wait_kv(cur + 1))) break;
+            if (!(ok = wait_k(cur + 1))) break;
             tc_fence_after();
-            issue_s(cur + 1, t_s, dq, dk, &bar_s_full);
+            issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
           }
           if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
-          const SmemDesc kst{dk_mn.lo + ((cur % NS) * S::kKVBytes >> 4), dk_mn.hi};
+          const SmemDesc kst{dk_mn.lo + ((cur % KS) * S::kKVBytes >> 4), dk_mn.hi};
           const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2)
             mma_ts(t_dq, t_dp + packed_col<kBN>(s2), kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
-          mma_commit(&bar_kv_empty[cur % NS]);
+          mma_commit(&bar_k_empty[cur % KS]);
           if (more) {
-            if (NS == 1) {
-              if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
-              if (!(ok = wait_kv(cur + 1))) break;
-              tc_fence_after();
-              issue_s(cur + 1, t_s, dq, dk, &bar_s_full);
-            }
-            issue_s(cur + 1, t_dp, ddo, dv, &bar_dp_full);
+            if (!(ok = wait_v(cur + 1))) break;
+            tc_fence_after();
+            issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
+            mma_commit(&bar_v_empty[(cur + 1) % VS]);
           }
         }
         if (!ok) break;
