@@ -472,9 +472,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ===========================================================================
 // Same role split as dK/dV: compute warp w owns query rows 32*(w%4).. and key
 // columns [(kBN/4)*(w/4), +kBN/4) of each step. TMEM: dQ at [0, kD), S at kColS,
-// dP at kColS + 128. The MMA thread issues  S_j, dP_j, | S_j+1, dQ_j, dP_j+1 | ...:
-// S_j+1 goes out as soon as the compute warps have read S_j into registers, dQ_j
-// once they have written dS_j (over their half of dP_j), dP_j+1 after dQ_j.
+// dP at kColDP and two packed 16-bit dS buffers at kColDS (step j uses buffer j%2).
+// The MMA thread stops twice per step: it issues S_j+1 once the compute warps have
+// read S_j, then dQ_j and dP_j+1 together once they have written dS_j. Every stop
+// between MMA groups (a wait, even a commit) leaves the tensor pipe idle for about
+// a hundred cycles, so the compute warps, which have slack, also do the K/V ring
+// bookkeeping: they check that the next K and V tiles have landed before they
+// arrive, and hand the stages back to the producer when the MMA commits show them
+// read.
 // K and V stream through separate rings: a K tile is read until dQ_j, late in
 // step j, and S_j+1 wants the next one early, so the K ring is the deeper one;
 // a V tile is free as soon as dP_j has read it.
@@ -491,7 +496,9 @@ struct DqShape {
   static constexpr int kSmemUsed = 2 * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
   static constexpr int kG = kBN / kColGroups;          // key columns per compute warp
-  static constexpr uint32_t kColDQ = 0, kColS = kD <= 128 ? 128 : 256, kColDP = kColS + 128;
+  static constexpr uint32_t kColDQ = 0, kColS = kD <= 128 ? 128 : 256, kColDP = kColS + kBN;
+  static constexpr uint32_t kColDS = kColDP + kBN, kDsCols = kBN / 2;  // two dS buffers
+  static_assert(kColDS + 2 * kDsCols <= 512, "TMEM budget");
   static_assert(kKStages >= 2 && kVStages >= 1, "shared memory budget");
 };
 
@@ -502,6 +509,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmV) {
   using S = DqShape<kD>;
   constexpr int kBN = S::kBN, KS = S::kKStages, VS = S::kVStages, kG = S::kG;
+  // With three or more K stages, K_j+1 can land while step j still holds K_j and
+  // K_j-1, so S_j+1 is issued as soon as S_j has been read; with two, K_j+1 reuses
+  // the stage of K_j-1, which dQ_j-1 frees only during step j, so S_j+1 goes out
+  // with dQ_j.
+  constexpr bool kEarlyS = KS >= 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -594,6 +606,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
       const uint32_t t_dq = tmem + S::kColDQ, t_s = tmem + S::kColS, t_dp = tmem + S::kColDP;
+      const uint32_t t_ds = tmem + S::kColDS;
       // Q, dO, K, V K-major for S / dP; K N-major (d-contiguous) for dS K.
       const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
       const SmemDesc ddo = smem_desc(smem_u32(sDO), 16, 1024, kLayoutSW128);
@@ -622,18 +635,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
         if (!(ok = wait_k(it))) break;
-        tc_fence_after();
-        issue_s(it % KS, t_s, dq, dk, &bar_s_full);
         if (!(ok = wait_v(it))) break;
         tc_fence_after();
+        issue_s(it % KS, t_s, dq, dk, &bar_s_full);
         issue_s(it % VS, t_dp, ddo, dv, &bar_dp_full);
-        mma_commit(&bar_v_empty[it % VS]);
+        // Two hand-overs per step. The compute warps arrive on s_free once they
+        // have read S_j and K_j+1 has landed, and on ds_ready once dS_j is written
+        // (dP_j read) and V_j+1 has landed; they also hand the K/V stages back to
+        // the producer, so this thread never stops for ring bookkeeping.
         for (int j = 0; j < n; ++j) {
           const int cur = it + j;
           const bool more = j + 1 < n;
-          if (more) {  // S_j+1 into the S buffer once S_j has been read (KS >= 2)
+          if (kEarlyS && more) {
             if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
-            if (!(ok = wait_k(cur + 1))) break;
             tc_fence_after();
             issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
           }
@@ -641,17 +655,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           const SmemDesc kst{dk_mn.lo + ((cur % KS) * S::kKVBytes >> 4), dk_mn.hi};
+          const uint32_t a_ds = t_ds + (cur & 1) * S::kDsCols;
           const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2)
-            mma_ts(t_dq, t_dp + packed_col<kBN>(s2), kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
-          mma_commit(&bar_k_empty[cur % KS]);
-          if (more) {
-            if (!(ok = wait_v(cur + 1))) break;
-            tc_fence_after();
-            issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
-            mma_commit(&bar_v_empty[(cur + 1) % VS]);
-          }
+            mma_ts(t_dq, a_ds + s2 * 8, kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
+          if (!kEarlyS && more) issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
+          // dp_full of step j+1 also covers dQ_j: K_j is free once it fires
+          if (more) issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
         }
         if (!ok) break;
         it += n;
@@ -693,6 +704,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if constexpr (kG == 32) tmem_ld32(tmem + S::kColS + lane_base + col0, sv);
           else tmem_ld16(tmem + S::kColS + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(sv));
           tmem_ld_wait();
+          if (kEarlyS && tid == 0 && j + 1 < n)
+            ok = mbar_wait(&bar_k_full[(it + 1) % KS], ((it + 1) / KS) & 1, status);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
           tc_fence_before();
           mbar_arrive(&bar_s_free);
           if (__all_sync(0xffffffffu, nvalid >= kG)) {
@@ -706,10 +721,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
         }
-        // ---- phase B: dS = P (dP - D), written over this warp's half of dP
+        // ---- phase B: dS = P (dP - D), packed into dS buffer it % 2
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_dp_full, it & 1, status));
         if (!ok) break;
         tc_fence_after();
+        if (tid == 0) {
+          // dP_it is done, so V stage it is free; past an item's first step the
+          // commit also covered dQ_(it-1), which was the last reader of K stage it-1.
+          mbar_arrive(&bar_v_empty[it % VS]);
+          if (j > 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);
+        }
         {
           uint32_t dv[kG];
           if constexpr (kG == 32) tmem_ld32(tmem + S::kColDP + lane_base + col0, dv);
@@ -720,10 +741,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int k = 0; k < kG / 2; ++k)
             dd[k] = pack2<kBF16>(pv[2 * k] * (__uint_as_float(dv[2 * k]) - dlt),
                                  pv[2 * k + 1] * (__uint_as_float(dv[2 * k + 1]) - dlt));
-          if constexpr (kG == 32) tmem_st16(tmem + S::kColDP + lane_base + col0, dd);
-          else tmem_st8(tmem + S::kColDP + lane_base + col0, *reinterpret_cast<uint32_t(*)[8]>(dd));
+          const uint32_t ds_col = S::kColDS + (it & 1) * S::kDsCols + grp * (kG / 2);
+          if constexpr (kG == 32) tmem_st16(tmem + ds_col + lane_base, dd);
+          else tmem_st8(tmem + ds_col + lane_base, *reinterpret_cast<uint32_t(*)[8]>(dd));
         }
         tmem_st_wait();
+        if (!kEarlyS && tid == 0 && j + 1 < n)
+          ok = mbar_wait(&bar_k_full[(it + 1) % KS], ((it + 1) / KS) & 1, status);
+        if (tid == 0 && j + 1 < n)
+          ok = ok && mbar_wait(&bar_v_full[(it + 1) % VS], ((it + 1) / VS) & 1, status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
         tc_fence_before();
         mbar_arrive(&bar_ds_ready);
       }
@@ -731,6 +759,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
+      if (tid == 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);  // dQ of the item's last step
       elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + gi * p.d;
       constexpr int kOutCols = kD / kColGroups;
 #pragma unroll
