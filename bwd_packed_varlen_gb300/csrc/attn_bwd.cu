@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         issue_st(it, t_st, dk, dq, &bar_s_full);
         issue_st(it, t_dpt, dv, ddo, &bar_dp_full);
+        // K and V are free once the item's last S^T and dP^T are done, so the next
+        // item's tiles load while its final dV/dK products still run.
+        if (I.steps == 1) mma_commit(&bar_kv_empty);
         for (int t = 0; t < I.steps; ++t) {
           const int cur = it + t;
           const bool more = t + 1 < I.steps;
@@ -315,11 +318,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               issue_st(cur + 1, t_st, dk, dq, &bar_s_full);
             }
             issue_st(cur + 1, t_dpt, dv, ddo, &bar_dp_full);
+            if (t + 2 == I.steps) mma_commit(&bar_kv_empty);
           }
         }
         if (!ok) break;
         it += I.steps;
-        mma_commit(&bar_kv_empty);
         mma_commit(&bar_acc_full);
       }
     }
@@ -639,6 +642,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         issue_s(it % KS, t_s, dq, dk, &bar_s_full);
         issue_s(it % VS, t_dp, ddo, dv, &bar_dp_full);
+        // Q and dO are free once the item's last S and dP are done: the next item's
+        // tiles then load while its final dQ steps still run.
+        if (n == 1) mma_commit(&bar_q_empty);
         // Two hand-overs per step. The compute warps arrive on s_free once they
         // have read S_j and K_j+1 has landed, and on ds_ready once dS_j is written
         // (dP_j read) and V_j+1 has landed; they also hand the K/V stages back to
@@ -663,10 +669,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!kEarlyS && more) issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
           // dp_full of step j+1 also covers dQ_j: K_j is free once it fires
           if (more) issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
+          if (j + 2 == n) mma_commit(&bar_q_empty);
         }
         if (!ok) break;
         it += n;
-        mma_commit(&bar_q_empty);
         mma_commit(&bar_acc_full);
       }
     }
