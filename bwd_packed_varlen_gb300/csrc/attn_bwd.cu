@@ -218,10 +218,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nxt = blockIdx.x;
       for (; ok; ++ii) {
         const int item = nxt < n_items ? nxt : -1;
-        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
-        nxt = next_item(p.header + kHdrNextDkdv);  // used at the next hand-over
-
+        if (item < 0) {
+          ok = ring_put(ring, ii, -1, status);
+          break;
+        }
         const Item I = decode(item);
+        // step count and column half travel with the item: the MMA thread then
+        // needs no global loads (which would queue behind the dK/dV row stores)
+        if (!(ok = ring_put(ring, ii, item, status, I.steps | (I.split << 24)))) break;
+        nxt = next_item(p.header + kHdrNextDkdv);  // used at the next hand-over
         if (ii > 0 && !(ok = mbar_wait(&bar_kv_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * S::kKVBytes);
         for (int c = 0; c < S::kChunks; ++c) {
@@ -281,11 +286,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int s = 0; s < kBM / 16; ++s)
           mma_ts(d_tmem, a_tmem + packed_col<kBM>(s), bst, s * 2048, idAcc, s > 0 ? 1u : acc0);
       };
+      struct {
+        int steps, split;
+      } I;
       for (; ok; ++ii) {
-        const int item = ring_get(ring, ii, status, &ok);
+        int aux = 0;
+        const int item = ring_get(ring, ii, status, &ok, &aux);
         if (!ok || item < 0) break;
-
-        const Item I = decode(item);
+        I.steps = aux & 0xffffff;
+        I.split = aux >> 24;
         if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
         const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
         if (!(ok = wait_q(it))) break;
@@ -576,13 +585,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nxt = blockIdx.x;
       for (; ok; ++ii) {
         const int item = nxt < n_items ? nxt : -1;
-        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
-        nxt = next_item(p.header + kHdrNextDq);  // used at the next hand-over
-
+        if (item < 0) {
+          ok = ring_put(ring, ii, -1, status);
+          break;
+        }
         const int2 pr = p.q_pairs[item / p.hq];
         const int h = item % p.hq, g = h / p.group;
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+        // the step count travels with the item: the MMA thread then needs no global loads
+        if (!(ok = ring_put(ring, ii, item, status, n))) break;
+        nxt = next_item(p.header + kHdrNextDq);  // used at the next hand-over
         if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_q_full, 2 * S::kQBytes);
         for (int c = 0; c < S::kChunks; ++c) {
@@ -630,12 +643,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(done);
       };
       for (; ok; ++ii) {
-        const int item = ring_get(ring, ii, status, &ok);
+        int n = 0;
+        const int item = ring_get(ring, ii, status, &ok, &n);
         if (!ok || item < 0) break;
-
-        const int2 pr = p.q_pairs[item / p.hq];
-        const SeqInfo s = load_seq(p, pr.x);
-        const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
         if (!(ok = wait_k(it))) break;
         if (!(ok = wait_v(it))) break;
@@ -681,23 +691,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int col0 = grp * kG;
     const float sl2 = p.scale_log2;
-    int it = 0, ii = 0;
-    bool ok = true;
-    for (; ok; ++ii) {
-      const int item = ring_get_warp(ring, ii, status, &ok);
-      if (!ok || item < 0) break;
-
+    // Per-item values of this thread's query row. The next item is decoded (its
+    // global loads issued) before this item's dQ rows are stored: loads queued
+    // behind those scattered row stores would otherwise wait for all of them.
+    struct RowItem {
+      int item, n, lim;
+      bool row_valid;
+      size_t gi;
+      float lse2, dlt;
+    };
+    auto decode = [&](int item) {
+      RowItem r{item, 0, 0, false, 0, 0.f, 0.f};
+      if (item < 0) return r;
       const int2 pr = p.q_pairs[item / p.hq];
       const int h = item % p.hq;
       const SeqInfo s = load_seq(p, pr.x);
-      const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+      r.n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
       const int row = pr.y * kBlockM + quarter * 32 + lane;
-      const bool row_valid = row < s.len_q;
-      const size_t gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
-      const size_t ti = tiled_index(p, pr.x, pr.y * kBlockM + quarter * 32 + lane, h);
-      const float lse2 = row_valid ? p.lse_t[ti] : 0.f;
-      const float dlt = row_valid ? p.delta_t[ti] : 0.f;
-      const int lim = row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
+      r.row_valid = row < s.len_q;
+      r.gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
+      const size_t ti = tiled_index(p, pr.x, row, h);
+      r.lse2 = r.row_valid ? p.lse_t[ti] : 0.f;
+      r.dlt = r.row_valid ? p.delta_t[ti] : 0.f;
+      r.lim = r.row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
+      return r;
+    };
+    int it = 0, ii = 0;
+    bool ok = true;
+    RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));
+    for (; ok && cur.item >= 0; ++ii) {
+      const int n = cur.n, lim = cur.lim;
+      const float lse2 = cur.lse2, dlt = cur.dlt;
       for (int j = 0; j < n; ++j, ++it) {
         const int nvalid = lim - (j * kBN + col0);
         // ---- phase A: P = exp2(S * scale * log2e - lse2) into registers, then free S
@@ -762,11 +786,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bar_ds_ready);
       }
       if (!ok) break;
+      const RowItem nxt = decode(ring_get_warp(ring, ii + 1, status, &ok));
+      if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
       if (tid == 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);  // dQ of the item's last step
-      elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + gi * p.d;
+      const bool row_valid = cur.row_valid;
+      elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + cur.gi * p.d;
       constexpr int kOutCols = kD / kColGroups;
 #pragma unroll
       for (int c = 0; c < kOutCols; c += 16) {
@@ -778,6 +805,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bar_acc_empty);
+      cur = nxt;
     }
   }
 

@@ -136,9 +136,15 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       int nxt = blockIdx.x;
       for (; ok; ++ii) {
         const int item = nxt < n_items ? nxt : -1;
-        if (!(ok = ring_put(ring, ii, item, status)) || item < 0) break;
-        nxt = next_item(p.header + kHdrNextFwd);  // used at the next hand-over
+        if (item < 0) {
+          ok = ring_put(ring, ii, -1, status);
+          break;
+        }
         const FwdItem I = fwd_item(p, item, causal);
+        // both tiles' key-tile counts travel with the item: the MMA thread then
+        // needs no global loads (which would queue behind the softmax warps' O stores)
+        if (!(ok = ring_put(ring, ii, item, status, I.n[0] | (I.n[1] << 16)))) break;
+        nxt = next_item(p.header + kHdrNextFwd);  // used at the next hand-over
         if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
         const int ntiles = I.n[1] > 0 ? 2 : 1;
         mbar_arrive_expect_tx(&bar_q_full, ntiles * S::kTileBytes);
@@ -185,10 +191,16 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         }
         mma_commit(&bar_s_full[x]);
       };
+      struct {
+        int n[2], nmax;
+      } I;
       for (int ii = 0; ok; ++ii) {
-        const int item = ring_get(ring, ii, status, &ok);
+        int counts = 0;
+        const int item = ring_get(ring, ii, status, &ok, &counts);
         if (!ok || item < 0) break;
-        const FwdItem I = fwd_item(p, item, causal);
+        I.n[0] = counts & 0xffff;
+        I.n[1] = counts >> 16;
+        I.nmax = I.n[0] > I.n[1] ? I.n[0] : I.n[1];
         if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
         if (!(ok = mbar_wait(&bar_k_full[it % NS], (it / NS) & 1, status))) break;
         tc_fence_after();
@@ -249,15 +261,33 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
     using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
     int ns = 0, no = 0;  // S hand-overs and items seen by this tile
     bool ok = true;
-    for (int ii = 0; ok; ++ii) {
-      const int item = ring_get_warp(ring, ii, status, &ok);
-      if (!ok || item < 0) break;
+    // Per-item values of this thread's query row. The next item is decoded (its
+    // global loads issued) before this item's O rows are stored: loads queued
+    // behind those scattered row stores would otherwise wait for all of them.
+    struct RowItem {
+      int item, n, lim;
+      bool row_valid;
+      size_t out_row;  // token * hq + head of this row
+    };
+    auto decode = [&](int item) {
+      RowItem r{item, 0, 0, false, 0};
+      if (item < 0) return r;
       const FwdItem I = fwd_item(p, item, causal);
-      const int n = I.n[x];
-      if (n == 0) continue;
+      r.n = I.n[x];
       const int row = (2 * I.u + x) * kBlockM + quarter * 32 + lane;
-      const bool row_valid = row < I.s.len_q;
-      const int lim = row_valid ? (causal ? min(I.s.len_k, row + 1) : I.s.len_k) : 0;
+      r.row_valid = row < I.s.len_q;
+      r.lim = r.row_valid ? (causal ? min(I.s.len_k, row + 1) : I.s.len_k) : 0;
+      r.out_row = static_cast<size_t>(I.s.off_q + row) * p.hq + I.h;
+      return r;
+    };
+    RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));
+    for (int ii = 0; ok && cur.item >= 0; ++ii) {
+      if (cur.n == 0) {
+        cur = decode(ring_get_warp(ring, ii + 1, status, &ok));
+        continue;
+      }
+      const int n = cur.n, lim = cur.lim;
+      const bool row_valid = cur.row_valid;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[x], ns & 1, status));
@@ -348,14 +378,15 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         m = m_new;
       }
       if (!ok) break;
+      const RowItem nxt = decode(ring_get_warp(ring, ii + 1, status, &ok));
+      if (!ok) break;
       // epilogue: O / l and lse for this row once the tile's last P V has landed
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full[x], no & 1, status));
       if (!ok) break;
       ++no;
       tc_fence_after();
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      T* orow = static_cast<T*>(p.out) +
-                (static_cast<size_t>(I.s.off_q + row) * p.hq + I.h) * static_cast<size_t>(p.d);
+      T* orow = static_cast<T*>(p.out) + cur.out_row * static_cast<size_t>(p.d);
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t o[32];
@@ -376,10 +407,10 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
           }
         }
       }
-      if (row_valid)
-        p.lse[static_cast<size_t>(I.s.off_q + row) * p.hq + I.h] = m * 0.69314718055994531f + logf(l);
+      if (row_valid) p.lse[cur.out_row] = m * 0.69314718055994531f + logf(l);
       tc_fence_before();
       mbar_arrive(&bar_o_empty[x]);
+      cur = nxt;
     }
   }
 

@@ -15,6 +15,7 @@ namespace teattn {
 
 struct WorkRing {
   int item[2];
+  int aux[2];  // optional per-item value the producer hands over with the item
   uint64_t full[2];
   uint64_t empty[2];
 };
@@ -28,22 +29,24 @@ __device__ __forceinline__ void ring_init(WorkRing& r, uint32_t consumers) {
 }
 
 // Producer (one thread): publish hand-over number k (item < 0 means "no more work").
-__device__ __forceinline__ bool ring_put(WorkRing& r, int k, int item, int* status) {
+__device__ __forceinline__ bool ring_put(WorkRing& r, int k, int item, int* status, int aux = 0) {
   const int s = k & 1;
   if (k >= 2 && !mbar_wait(&r.empty[s], ((k >> 1) - 1) & 1, status)) return false;
   *reinterpret_cast<volatile int*>(&r.item[s]) = item;
+  *reinterpret_cast<volatile int*>(&r.aux[s]) = aux;
   mbar_arrive(&r.full[s]);
   return true;
 }
 
 // Consumer (a single thread): item of hand-over k; *ok = false on a timed-out wait.
-__device__ __forceinline__ int ring_get(WorkRing& r, int k, int* status, bool* ok) {
+__device__ __forceinline__ int ring_get(WorkRing& r, int k, int* status, bool* ok, int* aux = nullptr) {
   const int s = k & 1;
   if (!mbar_wait(&r.full[s], (k >> 1) & 1, status)) {
     *ok = false;
     return -1;
   }
   const int item = *reinterpret_cast<volatile int*>(&r.item[s]);
+  if (aux) *aux = *reinterpret_cast<volatile int*>(&r.aux[s]);
   mbar_arrive(&r.empty[s]);
   return item;
 }
