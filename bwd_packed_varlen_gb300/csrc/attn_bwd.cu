@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "row_store.cuh"
 #include "sm103_ptx.cuh"
 #include "tmap.h"
 #include "work_queue.cuh"
@@ -47,42 +48,6 @@ __device__ __forceinline__ float ex2b(float x) {
 
 template <bool kBF16>
 using elem_t = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
-
-// Store 32 fp32 values (scaled) as 16-bit to row[c0 .. c0+32), columns < d only.
-template <bool kBF16>
-__device__ __forceinline__ void store_row32(elem_t<kBF16>* row, int c0, int d, const uint32_t (&v)[32],
-                                            float scale) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int col = c0 + q * 8;
-    if (col + 8 <= d) {
-      uint4 w;
-      w.x = pack2<kBF16>(__uint_as_float(v[q * 8 + 0]) * scale, __uint_as_float(v[q * 8 + 1]) * scale);
-      w.y = pack2<kBF16>(__uint_as_float(v[q * 8 + 2]) * scale, __uint_as_float(v[q * 8 + 3]) * scale);
-      w.z = pack2<kBF16>(__uint_as_float(v[q * 8 + 4]) * scale, __uint_as_float(v[q * 8 + 5]) * scale);
-      w.w = pack2<kBF16>(__uint_as_float(v[q * 8 + 6]) * scale, __uint_as_float(v[q * 8 + 7]) * scale);
-      *reinterpret_cast<uint4*>(row + col) = w;
-    }
-  }
-}
-
-// Store 16 fp32 values (scaled) as 16-bit to row[c0 .. c0+16), columns < d only.
-template <bool kBF16>
-__device__ __forceinline__ void store_row16(elem_t<kBF16>* row, int c0, int d, const uint32_t (&v)[16],
-                                            float scale) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int col = c0 + q * 8;
-    if (col + 8 <= d) {
-      uint4 w;
-      w.x = pack2<kBF16>(__uint_as_float(v[q * 8 + 0]) * scale, __uint_as_float(v[q * 8 + 1]) * scale);
-      w.y = pack2<kBF16>(__uint_as_float(v[q * 8 + 2]) * scale, __uint_as_float(v[q * 8 + 3]) * scale);
-      w.z = pack2<kBF16>(__uint_as_float(v[q * 8 + 4]) * scale, __uint_as_float(v[q * 8 + 5]) * scale);
-      w.w = pack2<kBF16>(__uint_as_float(v[q * 8 + 6]) * scale, __uint_as_float(v[q * 8 + 7]) * scale);
-      *reinterpret_cast<uint4*>(row + col) = w;
-    }
-  }
-}
 
 // ===========================================================================
 // dK / dV
@@ -447,10 +412,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool store = kv_row < seen_keys(I.s, causal);
-      elem_t<kBF16>* dk_row = static_cast<elem_t<kBF16>*>(p.dk) +
-                              (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
-      elem_t<kBF16>* dv_row = static_cast<elem_t<kBF16>*>(p.dv) +
-                              (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
+      const size_t kv_off = (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
+      const auto dk_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dk) + kv_off, store);
+      const auto dv_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dv) + kv_off, store);
       const int col_out = I.split * S::kDo;
       constexpr int kOutCols = S::kDo / kColGroups;
 #pragma unroll
@@ -460,10 +424,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld16(tmem + S::kColDK + lane_base + c0, a);
         tmem_ld16(tmem + S::kColDV + lane_base + c0, b);
         tmem_ld_wait();
-        if (store) {
-          store_row16<kBF16>(dk_row, col_out + c0, p.d, a, p.scale);
-          store_row16<kBF16>(dv_row, col_out + c0, p.d, b, 1.0f);
-        }
+        store_pair16<kBF16>(dk_rows, col_out + c0, p.d, a, p.scale);
+        store_pair16<kBF16>(dv_rows, col_out + c0, p.d, b, 1.0f);
       }
       tc_fence_before();
       mbar_arrive(&bar_acc_empty);
@@ -792,8 +754,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (tid == 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);  // dQ of the item's last step
-      const bool row_valid = cur.row_valid;
-      elem_t<kBF16>* dq_row = static_cast<elem_t<kBF16>*>(p.dq) + cur.gi * p.d;
+      const auto rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dq) + cur.gi * p.d, cur.row_valid);
       constexpr int kOutCols = kD / kColGroups;
 #pragma unroll
       for (int c = 0; c < kOutCols; c += 16) {
@@ -801,7 +762,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t a[16];
         tmem_ld16(tmem + S::kColDQ + lane_base + c0, a);
         tmem_ld_wait();
-        if (row_valid) store_row16<kBF16>(dq_row, c0, p.d, a, p.scale);
+        store_pair16<kBF16>(rows, c0, p.d, a, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&bar_acc_empty);

@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "row_store.cuh"
 #include "sm103_ptx.cuh"
 #include "tmap.h"
 #include "work_queue.cuh"
@@ -386,26 +387,14 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       ++no;
       tc_fence_after();
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      T* orow = static_cast<T*>(p.out) + cur.out_row * static_cast<size_t>(p.d);
+      const auto rows = make_row_pair(static_cast<T*>(p.out) + cur.out_row * static_cast<size_t>(p.d), row_valid);
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(t_o + c0, o);
         tmem_ld_wait();
-        if (row_valid) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int col = c0 + v * 8;
-            if (col + 8 <= p.d) {
-              uint4 w;
-              w.x = pack2<kBF16>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
-              w.y = pack2<kBF16>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
-              w.z = pack2<kBF16>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
-              w.w = pack2<kBF16>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + col) = w;
-            }
-          }
-        }
+        store_pair16<kBF16>(rows, c0, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[0]), inv);
+        store_pair16<kBF16>(rows, c0 + 16, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[16]), inv);
       }
       if (row_valid) p.lse[cur.out_row] = m * 0.69314718055994531f + logf(l);
       tc_fence_before();
