@@ -9,15 +9,21 @@ float32, rounded once to the storage dtype, and returned as CPU torch tensors, s
 given seed yields the same bits on any machine. The recipes restate the workloads
 of the TransformerEngine issues this library addresses:
 
-``tiny_gqa``      issue #2448 reproduction (THD + GQA, fp16, d=8, padded to [0,4,12]).
-``packings``      issue #3333 reproduction (bf16 H=8 d=128 padding_causal, sum loss).
-``gqa_d256``      issue #3216 shape ([384,2,16,256] sbhd == 2 x 384 THD, hq=16,
+``tiny_gqa``      [2448] reproduction (THD + GQA, fp16, d=8, padded to [0,4,12]).
+``packings``      [3333] reproduction (bf16 H=8 d=128 padding_causal, sum loss).
+``gqa_d256``      [3216] shape ([384,2,16,256] sbhd == 2 x 384 THD, hq=16,
                   hkv=2, causal), with a synthetic peaked-softmax stand-in for the
                   captured activations that page attaches.
-``real_ne_padded`` issue #2892 reproduction (real [100,150,120,130] in padded
+``real_ne_padded`` [2892] reproduction (real [100,150,120,130] in padded
                   [112,160,128,144] slots, 32 heads, d=48), pad slots +-1e3.
 ``throughput``    32768 real tokens in seeded lengths in [256, 8192] padded to a
                   multiple of 64; hq=32, hkv=8, d=128, padding_causal.
+
+Pages cited, by title (keys are the pages' issue numbers):
+  [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+  [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
 """
 
 from __future__ import annotations
@@ -96,7 +102,7 @@ def _to(x: np.ndarray, dtype: str) -> torch.Tensor:
 
 
 def tiny_gqa(call: str = "A", seed: int = 42) -> Workload:
-    """Issue #2448: 12 token slots padded as [0,4,12]; call A has query lengths
+    """[2448]: 12 token slots padded as [0,4,12]; call A has query lengths
     (1, 2) and key lengths (3, 6); call B has query lengths (0, 3). The same q, k,
     v, dout feed both calls, so A;B versus B;A isolates call-order effects."""
     rng = np.random.default_rng(seed)
@@ -120,7 +126,7 @@ PACKINGS = ([128], [128, 96], [128, 128], [256, 256])
 
 
 def packings(lengths=(128,), seed: int = 42, H: int = 8, d: int = 128) -> Workload:
-    """Issue #3333: bf16, H=8 heads (MHA), d=128, padding_causal, cu == cu_padded,
+    """[3333]: bf16, H=8 heads (MHA), d=128, padding_causal, cu == cu_padded,
     upstream gradient of the sum loss (dout = ones)."""
     rng = np.random.default_rng(seed)
     T = int(sum(lengths))
@@ -138,7 +144,7 @@ def packings(lengths=(128,), seed: int = 42, H: int = 8, d: int = 128) -> Worklo
 def gqa_d256(seed: int = 3216, seq: int = 384, batch: int = 2, hq: int = 16,
              hkv: int = 2, d: int = 256, outlier: float = 20.0,
              outlier_mode: str = "set") -> Workload:
-    """Issue #3216 shape as THD: ``batch`` causal sequences of ``seq`` tokens,
+    """[3216] shape as THD: ``batch`` causal sequences of ``seq`` tokens,
     hq=16, hkv=2, d=256, scale 1/sqrt(d). q and k are N(0,1) times a per-channel
     lognormal(0,1) scale (drawn separately for q and k); the same 4 seeded outlier
     channels get scale ``outlier`` (20, i.e. 20x the median channel scale of 1) in
@@ -172,7 +178,7 @@ def gqa_d256(seed: int = 3216, seq: int = 384, batch: int = 2, hq: int = 16,
 def real_ne_padded(seed: int = 2892, mask_type: int = MASK_PADDING,
                    real=(100, 150, 120, 130), padded=(112, 160, 128, 144),
                    H: int = 32, d: int = 48, pad_value: float = 1e3) -> Workload:
-    """Issue #2892: real lengths [100,150,120,130] inside padded slots
+    """[2892]: real lengths [100,150,120,130] inside padded slots
     [112,160,128,144] (544 rows), 32 heads, d=48, hq=hkv. Real tokens are N(0,1);
     pad slots of q, k, v and dout hold +-pad_value with a seeded random sign, so any
     leak of a pad slot into a real output is large."""

@@ -2,6 +2,12 @@
  * te_attn.h -- C ABI of libteattn.so: scaled-dot-product attention forward and
  * backward over packed variable-length (THD) sequences, for NVIDIA GB300 (sm_103a).
  *
+ * Pages cited, by title (keys are the pages' issue numbers):
+ *   [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+ *   [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+ *   [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+ *   [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
+ *
  * What is computed (the TransformerEngine issues this library answers):
  *   For each sequence b and query head h (key/value head g = h / (hq / hkv)):
  *     S   = attn_scale * Q_b,h K_b,g^T        masked by the REAL lengths
@@ -10,11 +16,11 @@
  *   and the gradient of sum(dO * O):
  *     dV  = sum_{h in group} P^T dO,   dP = dO V^T,   D = rowsum(dO * O)
  *     dS  = P * (dP - D),  dQ = attn_scale dS K,  dK = attn_scale sum_{h in group} dS^T Q
- *   -- issue #2448 (THD + GQA fused_attn_bwd, "Expected behavior": rows of an empty
+ *   -- [2448] (THD + GQA fused_attn_bwd, "Expected behavior": rows of an empty
  *      query sequence give exactly-zero dk/dv, results must not depend on earlier
- *      calls), issue #3333 (THD padding_causal backward vs a per-sequence SDPA
- *      reference), issue #3216 (GQA via repeat_interleave, causal = upper-left
- *      triangle, head_dim 256 with batch >= 2), issue #2892 ("Expected Behavior":
+ *      calls), [3333] (THD padding_causal backward vs a per-sequence SDPA
+ *      reference), [3216] (GQA via repeat_interleave, causal = upper-left
+ *      triangle, head_dim 256 with batch >= 2), [2892] ("Expected Behavior":
  *      cu_seqlens_* mask, cu_seqlens_*_padded index memory, output keeps the padded
  *      layout).
  *
@@ -98,8 +104,8 @@ size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
 
 /*
  * Forward: writes out [total_q, hq, d] and lse [total_q, hq] (natural-log softmax
- * denominator of the scaled scores, fp32). Issue #2892 "Expected Behavior" fixes the
- * real/padded split; issue #2448 passes lse to the backward as the aux tensor.
+ * denominator of the scaled scores, fp32). [2892] "Expected Behavior" fixes the
+ * real/padded split; [2448] passes lse to the backward as the aux tensor.
  */
 int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, float* lse,
                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
@@ -113,7 +119,7 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
  * Backward: from q, k, v, out, dout and lse, writes dq [total_q, hq, d],
  * dk and dv [total_kv, hkv, d]. dk/dv of a key/value head sum over the hq/hkv query
  * heads of its group inside one thread block (no atomics). The arguments mirror
- * TransformerEngine's fused_attn_bwd as issue #2448 calls it (out and lse are
+ * TransformerEngine's fused_attn_bwd as [2448] calls it (out and lse are
  * inputs; dropout 0; no bias; deterministic).
  */
 int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out,

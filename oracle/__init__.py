@@ -11,18 +11,24 @@ online softmax and no fusion. The pages this follows (TransformerEngine issues o
 packed-sequence attention) fix:
 
 * real ``cu_seqlens_q/kv`` drive the masks and padded ``cu_seqlens_*_padded`` drive
-  the memory offsets; the output keeps the padded layout (issue #2892, "Expected
+  the memory offsets; the output keeps the padded layout ([2892], "Expected
   Behavior", items 1-3);
-* GQA maps query head h to key/value head h // (hq // hkv) (issue #3216,
+* GQA maps query head h to key/value head h // (hq // hkv) ([3216],
   ``fp32_reference`` with ``repeat_interleave``);
 * the causal mask is the upper-left triangle, key j visible to query i iff j <= i
-  (issue #3216, ``torch.triu(..., 1)`` filled with -inf);
-* rows that hold no token of any sequence get exactly-zero gradients (issue #2448,
+  ([3216], ``torch.triu(..., 1)`` filled with -inf);
+* rows that hold no token of any sequence get exactly-zero gradients ([2448],
   "Expected behavior": the first 4 tokens of dk/dv are zero when the first query
   sequence is empty).
 
 Parity status of each function is stated in its docstring; all are pinned by the
 ``-m "not gpu"`` tests in ``tests/test_oracle.py``.
+
+Pages cited, by title (keys are the pages' issue numbers):
+  [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+  [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
 """
 
 from .attention import (  # noqa: F401

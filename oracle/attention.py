@@ -5,21 +5,21 @@ TEST INFRASTRUCTURE ONLY (see the package docstring): the CUDA path never import
 Notation follows the TransformerEngine pages this oracle restates:
 
 * ``q, out, dout, dq`` are ``[T_q, hq, d]``; ``k, v, dk, dv`` are ``[T_kv, hkv, d]``;
-  ``lse`` is ``[T_q, hq]`` (issue #2448, reproduction script: THD tensors
+  ``lse`` is ``[T_q, hq]`` ([2448], reproduction script: THD tensors
   ``(seqlen, heads, dim)`` and the softmax aux tensor ``(seqlen, hq, 1)``).
 * Sequence b occupies rows ``cu_*_padded[b] .. cu_*_padded[b+1]`` of its tensor and
-  holds ``cu_*[b+1] - cu_*[b]`` real tokens at the front of that span (issue #2892,
+  holds ``cu_*[b+1] - cu_*[b]`` real tokens at the front of that span ([2892],
   "Expected Behavior": real boundaries mask, padded boundaries index memory).
-* Query head h reads key/value head ``h // G`` with ``G = hq // hkv`` (issue #3216,
+* Query head h reads key/value head ``h // G`` with ``G = hq // hkv`` ([3216],
   ``fp32_reference``: ``repeat_interleave`` of K/V over the group), so dK/dV of a
   key/value head are sums over the G query heads of its group.
-* ``attn_scale`` multiplies ``q k^T`` inside the softmax (issue #2448 passes
-  ``attn_scale=0.1``; issue #3216 divides by sqrt(d)); ``lse`` is the natural log of
+* ``attn_scale`` multiplies ``q k^T`` inside the softmax ([2448] passes
+  ``attn_scale=0.1``; [3216] divides by sqrt(d)); ``lse`` is the natural log of
   the softmax denominator of the *scaled* scores.
 * ``padding_causal`` keeps key j for query i iff ``j <= i`` (upper-left alignment,
-  issue #3216 ``torch.triu(ones, 1)`` masked to -inf).
+  [3216] ``torch.triu(ones, 1)`` masked to -inf).
 
-Readings where the pages are silent (each is listed in the design doc as well):
+Readings where the pages are silent:
 
 * A valid query whose sequence has no valid key gets ``out = 0``, ``lse = -inf`` and
   ``dq = 0`` (empty-sum convention).
@@ -27,8 +27,14 @@ Readings where the pages are silent (each is listed in the design doc as well):
   exactly 0 in ``out, dq`` and ``lse``; key/value rows that are not real tokens, or
   that no valid query sees, are exactly 0 in ``dk, dv``.
 * The backward entry takes ``out`` and ``lse`` as inputs, as TransformerEngine's
-  ``fused_attn_bwd`` does (issue #2448 passes ``out`` and ``[lse, rng]``), and forms
+  ``fused_attn_bwd`` does ([2448] passes ``out`` and ``[lse, rng]``), and forms
   ``P = exp(S - lse)`` and ``D = rowsum(dout * out)`` from them.
+
+Pages cited, by title (keys are the pages' issue numbers):
+  [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+  [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
 """
 
 from __future__ import annotations
@@ -50,7 +56,7 @@ def _is_causal(mask_type) -> bool:
 
 def seq_spans(cu_seqlens, cu_seqlens_padded):
     """Per sequence ``(offset, real_length)``: offset from the padded prefix sums,
-    length from the real ones (issue #2892, "Expected Behavior", items 1-2)."""
+    length from the real ones ([2892], "Expected Behavior", items 1-2)."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     cp = np.asarray(cu_seqlens_padded, dtype=np.int64)
     if cu.shape != cp.shape or cu.ndim != 1 or cu.size < 2:
@@ -77,9 +83,9 @@ def attn_group_fwd_bwd(qg, kg, vg, dog, scale, causal):
     ``qg, dog``: ``[Lq, G, d]``; ``kg, vg``: ``[Lk, d]``. Returns
     ``(out [Lq,G,d], lse [Lq,G], dq [Lq,G,d], dk [Lk,d], dv [Lk,d])``.
 
-    Forward is the softmax-attention definition (issue #3216 ``fp32_reference``:
+    Forward is the softmax-attention definition ([3216] ``fp32_reference``:
     ``softmax(q k^T / sqrt(d)) v`` with the causal triangle). Backward is the
-    gradient of ``sum(dout * out)`` (issues #3333 and #3216 obtain their reference
+    gradient of ``sum(dout * out)`` ([3333] and [3216] obtain their reference
     gradients by autograd of this loss): ``dV = P^T dO``, ``dP = dO V^T``,
     ``D_i = sum_j P_ij dP_ij``, ``dS = P (dP - D)``, ``dQ = scale dS K``,
     ``dK = scale dS^T Q``, summed over the G query heads for dK and dV.
@@ -123,7 +129,7 @@ def attn_group_bwd_given(qg, kg, vg, outg, dog, lseg, scale, causal):
     """Backward for one sequence and key/value group from a supplied ``out``/``lse``.
 
     This is the interface TransformerEngine's ``fused_attn_bwd`` exposes (issue
-    #2448 reproduction: ``q, k, v, out, dout`` plus the aux tensor ``lse``):
+    [2448] reproduction: ``q, k, v, out, dout`` plus the aux tensor ``lse``):
     ``P = exp(S - lse)``, ``D = rowsum(dout * out)``, then the same products as
     :func:`attn_group_fwd_bwd`. When ``out, lse`` are the exact forward results the
     two functions agree (``sum_j P_ij dP_ij = dO_i . O_i``).
@@ -168,8 +174,8 @@ def attn_fwd_bwd_thd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv,
     """THD forward + backward: ``(out, lse, dq, dk, dv)`` in float64, padded layout.
 
     Loops over sequences and key/value heads and calls :func:`attn_group_fwd_bwd`
-    on the real rows; every other row stays exactly 0 (issue #2448 "Expected
-    behavior"; issue #2892: output keeps the padded shape of Q).
+    on the real rows; every other row stays exactly 0 ([2448] "Expected
+    behavior"; [2892]: output keeps the padded shape of Q).
     Parity: pinned.
     """
     causal = _is_causal(mask_type)
@@ -217,7 +223,7 @@ def attn_bwd_thd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv,
                  cu_seqlens_q_padded, cu_seqlens_kv_padded, attn_scale, mask_type):
     """THD backward from supplied ``out`` and ``lse``: ``(dq, dk, dv)`` float64.
 
-    The interface of TransformerEngine's ``fused_attn_bwd`` (issue #2448
+    The interface of TransformerEngine's ``fused_attn_bwd`` ([2448]
     reproduction). Rows that are not real tokens, and key/value rows that no valid
     query sees, are exactly 0.
     Parity: pinned."""
@@ -253,8 +259,8 @@ def valid_row_masks(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
     one real key; a key/value row may be nonzero in dk/dv iff it is a real token that
     some real query sees (padding: the sequence has a query; padding_causal: also
     its index is below the query length, since query i sees keys j <= i).
-    Every other row must be exactly 0 (issue #2448 "Expected behavior").
-    Parity: pinned by the golden fixtures of issues #2448 and #2892.
+    Every other row must be exactly 0 ([2448] "Expected behavior").
+    Parity: pinned by the golden fixtures of [2448] and [2892].
     """
     causal = _is_causal(mask_type)
     qs = seq_spans(cu_seqlens_q, cu_seqlens_q_padded)

@@ -1,6 +1,13 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle on the
 workloads of the TransformerEngine pages, ragged edge cases, and the determinism
-requirements (call order, buffer contents, allocator churn)."""
+requirements (call order, buffer contents, allocator churn).
+
+Pages cited, by title (keys are the pages' issue numbers):
+  [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+  [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
+"""
 
 import numpy as np
 import pytest
@@ -30,7 +37,7 @@ def _lib():
 
 
 def test_tiny_gqa_call_order_and_zero_rows():
-    """Issue #2448: calls A then B and B then A give identical results, and in call B
+    """[2448]: calls A then B and B then A give identical results, and in call B
     (empty first query sequence) dk/dv rows 0-3 are exactly zero."""
     wa, wb = W.tiny_gqa("A"), W.tiny_gqa("B")
     ta, tb = to_dev(wa), to_dev(wb)
@@ -49,20 +56,20 @@ def test_tiny_gqa_call_order_and_zero_rows():
 
 @pytest.mark.parametrize("lengths", W.PACKINGS, ids=lambda x: "_".join(map(str, x)))
 def test_packings(lengths):
-    """Issue #3333 packings: bf16, 8 heads, d=128, padding_causal, sum loss."""
+    """[3333] packings: bf16, 8 heads, d=128, padding_causal, sum loss."""
     w = W.packings(list(lengths))
     check_against_oracle(w, gpu_fwd_bwd(w))
 
 
 def test_gqa_d256_peaked():
-    """Issue #3216 shape: 2 x 384 causal, hq=16, hkv=2, d=256, peaked softmax."""
+    """[3216] shape: 2 x 384 causal, hq=16, hkv=2, d=256, peaked softmax."""
     w = W.gqa_d256()
     check_against_oracle(w, gpu_fwd_bwd(w))
 
 
 @pytest.mark.parametrize("mask", [W.MASK_PADDING, W.MASK_PADDING_CAUSAL])
 def test_real_ne_padded(mask):
-    """Issue #2892: real lengths inside larger padded slots filled with +-1e3; the
+    """[2892]: real lengths inside larger padded slots filled with +-1e3; the
     output keeps the padded layout and pad rows are exactly zero."""
     w = W.real_ne_padded(mask_type=mask)
     res = gpu_fwd_bwd(w)
@@ -147,7 +154,7 @@ def test_all_sequences_empty_and_keyless():
 def test_bitwise_repeatable_and_poisoned_buffers():
     """Outputs are bit-identical across repeated calls, with output and workspace
     buffers pre-filled with NaN bytes, and after allocator churn between calls
-    (the workspace-reuse failure of issue #2448)."""
+    (the workspace-reuse failure of [2448])."""
     import bwd_packed_varlen_gb300 as ta
     w = W.random_varlen(40, 4, 700, 8, 2, 128, W.MASK_PADDING_CAUSAL, "bf16")
     t = to_dev(w)

@@ -3,6 +3,12 @@
 Each test fixes the oracle to an independent fact: finite differences of the loss,
 torch's own float64 SDPA + autograd, closed forms, algebraic invariants, and the
 layouts and zero rows that the TransformerEngine pages state (tests/golden/).
+
+Pages cited, by title (keys are the pages' issue numbers):
+  [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3333] "[Bug] FusedAttention (cuDNN) THD backward produces wrong gradients on sm_120 (RTX 5090); forward is correct, Unfused is correct"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
+  [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
 """
 
 import json
@@ -70,7 +76,7 @@ def test_finite_differences(mask):
 
 def _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, causal):
     """Per-sequence torch float64 SDPA (math) + autograd with repeat_interleave GQA,
-    the reference construction of issues #3333 and #3216."""
+    the reference construction of [3333] and [3216]."""
     hq, hkv = q.shape[1], k.shape[1]
     G = hq // hkv
     tq = torch.tensor(q, requires_grad=True)
@@ -314,7 +320,7 @@ def test_exact_zero_rows(mask):
 
 
 def test_golden_issue2448_zero_rows():
-    """Issue #2448 'Expected behavior': on the second call (query lengths 0 and 3)
+    """[2448] 'Expected behavior': on the second call (query lengths 0 and 3)
     the first 4 tokens of dk and dv are all zero; on the first they are not."""
     g = json.load(open(os.path.join(GOLDEN, "issue2448_expected_zero_rows.json")))
     rng = np.random.default_rng(0)
@@ -335,7 +341,7 @@ def test_golden_issue2448_zero_rows():
 
 
 def test_golden_issue2892_layout():
-    """Issue #2892 / TE docstring: real [0,3,5,9] in padded [0,4,8,13]; the output
+    """[2892] / TE docstring: real [0,3,5,9] in padded [0,4,8,13]; the output
     keeps the padded shape, real rows carry values, pad rows are zero."""
     g = json.load(open(os.path.join(GOLDEN, "issue2892_te_docstring_layout.json")))
     rng = np.random.default_rng(1)
