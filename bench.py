@@ -357,19 +357,52 @@ def run_ours(args, rank, world, local_rank):
         d2h = sum(x.numel() * x.element_size() for x in host_out)
         es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        # Each step copies its own inputs in and its own results out; copies run on
+        # two copy streams and overlap the step's compute where the data allow it:
+        # dout travels while the forward runs, out/lse travel back while the
+        # backward runs. Nothing crosses a step boundary (the step's end event waits
+        # for its last device-to-host copy).
+        main = torch.cuda.current_stream(dev)
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+        fwd_in = ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_kv", "cu_seqlens_q_padded",
+                  "cu_seqlens_kv_padded")
+        cus_d = (dev_in["cu_seqlens_q"], dev_in["cu_seqlens_kv"], dev_in["cu_seqlens_q_padded"],
+                 dev_in["cu_seqlens_kv_padded"])
         barrier()
         torch.cuda.synchronize()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            es[i].record()
-            for k_, v_ in host_in.items():
-                dev_in[k_].copy_(v_, non_blocking=True)
-            step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["dout"],
-                 (dev_in["cu_seqlens_q"], dev_in["cu_seqlens_kv"], dev_in["cu_seqlens_q_padded"],
-                  dev_in["cu_seqlens_kv_padded"]))
-            for ho, dx in zip(host_out, (out, lse, dq, dk, dv)):
-                ho.copy_(dx, non_blocking=True)
-            ee[i].record()
+            es[i].record(main)
+            s_in.wait_stream(main)
+            with torch.cuda.stream(s_in):
+                for k_ in fwd_in:
+                    dev_in[k_].copy_(host_in[k_], non_blocking=True)
+                ev_fwd_in = torch.cuda.Event()
+                ev_fwd_in.record(s_in)
+                dev_in["dout"].copy_(host_in["dout"], non_blocking=True)
+                ev_bwd_in = torch.cuda.Event()
+                ev_bwd_in.record(s_in)
+            main.wait_event(ev_fwd_in)
+            ta.fwd(dev_in["q"], dev_in["k"], dev_in["v"], *cus_d, w.attn_scale, w.mask_type,
+                   w.max_seqlen_q, w.max_seqlen_kv, out=out, lse=lse, workspace=wsf)
+            ev_fwd = torch.cuda.Event()
+            ev_fwd.record(main)
+            main.wait_event(ev_bwd_in)
+            ta.bwd(dev_in["q"], dev_in["k"], dev_in["v"], out, dev_in["dout"], lse, *cus_d,
+                   w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk, dv=dv,
+                   workspace=wsb)
+            ev_bwd = torch.cuda.Event()
+            ev_bwd.record(main)
+            s_out.wait_event(ev_fwd)
+            with torch.cuda.stream(s_out):
+                host_out[0].copy_(out, non_blocking=True)
+                host_out[1].copy_(lse, non_blocking=True)
+                s_out.wait_event(ev_bwd)
+                for ho, dx in zip(host_out[2:], (dq, dk, dv)):
+                    ho.copy_(dx, non_blocking=True)
+            main.wait_stream(s_out)
+            ee[i].record(main)
         torch.cuda.synchronize()
         barrier()
         ems = sum(a.elapsed_time(b) for a, b in zip(es, ee)) / args.steps
