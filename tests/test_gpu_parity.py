@@ -258,3 +258,45 @@ def test_throughput_workload_sampled():
         assert_close(f"dq[{b},{g}]", dq[oq:oq + L, hs], r[2])
         assert_close(f"dk[{b},{g}]", dk[oq:oq + L, g], r[3])
         assert_close(f"dv[{b},{g}]", dv[oq:oq + L, g], r[4])
+
+
+def test_issue3333_reference_norms_from_page_rng():
+    """[3333] "Reproduction" / "Results": q, k, v drawn exactly as the page's script
+    draws them (torch.manual_seed(42), three bf16 torch.randn(total, 8, 128) on the
+    GPU), per-sequence causal attention, loss = sum(out). The page prints the norm
+    of the fp32 reference query gradient to two decimals: 74.97, 101.93, 104.96,
+    126.25. The oracle's dQ norm must print the same for the packings of up to 256
+    tokens, and the CUDA path's must match the oracle for all four. For the 512-token
+    packing the generator's stream appears to depend on the GPU, so a
+    different norm there is reported, not failed; if even the first packing does not
+    reproduce, this GPU's generator differs and the pin is skipped."""
+    import json
+    import os
+
+    import bwd_packed_varlen_gb300 as ta
+
+    fx = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "issue3333_qgrad_norms.json")))
+    results = []
+    for lengths, ref_norm in zip(fx["lengths"], fx["ref_qgrad_norm"]):
+        total = sum(lengths)
+        torch.manual_seed(42)
+        q, k, v = (torch.randn(total, 8, 128, device="cuda", dtype=torch.bfloat16) for _ in range(3))
+        dout = torch.ones_like(q)
+        offs = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        cu = torch.tensor(offs, dtype=torch.int32).cuda()
+        scale = 1.0 / np.sqrt(128.0)
+        _, _, dq_ref, _, _ = oracle.attn_fwd_bwd_thd(
+            np64(q), np64(k), np64(v), np64(dout), offs, offs, offs, offs, scale, W.MASK_PADDING_CAUSAL)
+        norm = float(np.linalg.norm(dq_ref))
+        out, lse = ta.fwd(q, k, v, cu, cu, cu, cu, scale, W.MASK_PADDING_CAUSAL, max(lengths), max(lengths))
+        dq, _, _ = ta.bwd(q, k, v, out, dout, lse, cu, cu, cu, cu, scale, W.MASK_PADDING_CAUSAL,
+                          max(lengths), max(lengths))
+        torch.cuda.synchronize()
+        gnorm = float(np.linalg.norm(np64(dq)))
+        assert abs(gnorm - norm) <= 1e-2 * norm, (lengths, gnorm, norm)
+        results.append((lengths, total, norm, ref_norm, abs(norm - ref_norm) <= 0.006))
+    if not results[0][4]:
+        pytest.skip(f"this GPU's generator does not reproduce the page's stream: {results}")
+    bad = [r for r in results if r[1] <= 256 and not r[4]]
+    assert not bad, f"page norms not reproduced: {bad} (all: {results})"
+    print("issue 3333 norms (lengths, tokens, oracle, page, reproduced):", results)
