@@ -1,7 +1,10 @@
 // Backward attention over packed variable-length sequences on sm_103a.
 //
-// Two tensor-core kernels, both with the role split of the forward kernel
-// (warp 4 TMA, warp 5 one MMA-issuing thread, warps 0-3 one thread per TMEM lane):
+// Two persistent tensor-core kernels with the same role split: 16 compute warps
+// (warp w owns TMEM lane quarter w % 4 and a quarter of the step's columns), one
+// TMA producer warp and one warp whose lane 0 issues every tcgen05.mma. Work items
+// come from the scheduler's sorted lists through a per-kernel counter and a
+// shared-memory ring (see work_queue.cuh).
 //
 // dK/dV kernel -- item = (sequence b, key/value head g, 128-row key tile).
 //   K and V of the tile stay in shared memory for the whole item; the item sweeps
@@ -18,8 +21,9 @@
 //   produces half of the output columns (two blocks per item).
 //
 // dQ kernel -- item = (sequence b, query head h, 128-row query tile); Q and dO stay
-//   in shared memory, key tiles stream: S = Q K^T, dP = dO V^T, dS = P (dP - D),
-//   dQ += dS K with dQ in TMEM.
+//   in shared memory, key tiles stream through separate K and V rings: S = Q K^T,
+//   dP = dO V^T, dS = P (dP - D) into one of two 16-bit TMEM buffers, dQ += dS K
+//   with dQ in TMEM.
 //
 // Both scale by attn_scale in the epilogue and store only rows that belong to
 // real tokens (and, for dK/dV, that some real query sees); every other row is

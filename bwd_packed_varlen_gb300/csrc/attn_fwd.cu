@@ -1,4 +1,6 @@
-// Forward attention over packed variable-length sequences on sm_103a.
+// Forward attention over packed variable-length sequences on sm_103a, one query
+// tile per work item (used for head_dim 256; head_dim <= 128 runs the two-tile
+// kernel in attn_fwd_pair.cu).
 //
 // One work item = (sequence b, query head h, 128-row query tile). A persistent
 // grid walks the scheduler's sorted item list with a static stride. Inside a
