@@ -360,8 +360,9 @@ def run_ours(args, rank, world, local_rank):
         # Each step copies its own inputs in and its own results out; copies run on
         # two copy streams and overlap the step's compute where the data allow it:
         # dout travels while the forward runs, out/lse travel back while the
-        # backward runs. Nothing crosses a step boundary (the step's end event waits
-        # for its last device-to-host copy).
+        # backward runs, dq travels back while dk/dv are computed (the backward's
+        # dq hand-over event). Nothing crosses a step boundary (the step's end
+        # event waits for its last device-to-host copy).
         main = torch.cuda.current_stream(dev)
         s_in = torch.cuda.Stream(device=dev)
         s_out = torch.cuda.Stream(device=dev)
@@ -389,18 +390,21 @@ def run_ours(args, rank, world, local_rank):
             ev_fwd = torch.cuda.Event()
             ev_fwd.record(main)
             main.wait_event(ev_bwd_in)
+            ev_dq = torch.cuda.Event()
             ta.bwd(dev_in["q"], dev_in["k"], dev_in["v"], out, dev_in["dout"], lse, *cus_d,
                    w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk, dv=dv,
-                   workspace=wsb)
+                   workspace=wsb, dq_done=ev_dq)
             ev_bwd = torch.cuda.Event()
             ev_bwd.record(main)
             s_out.wait_event(ev_fwd)
             with torch.cuda.stream(s_out):
                 host_out[0].copy_(out, non_blocking=True)
                 host_out[1].copy_(lse, non_blocking=True)
+                s_out.wait_event(ev_dq)
+                host_out[2].copy_(dq, non_blocking=True)
                 s_out.wait_event(ev_bwd)
-                for ho, dx in zip(host_out[2:], (dq, dk, dv)):
-                    ho.copy_(dx, non_blocking=True)
+                host_out[3].copy_(dk, non_blocking=True)
+                host_out[4].copy_(dv, non_blocking=True)
             main.wait_stream(s_out)
             ee[i].record(main)
         torch.cuda.synchronize()

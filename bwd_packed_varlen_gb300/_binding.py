@@ -56,6 +56,8 @@ def library() -> ctypes.CDLL:
     L.te_attn_fwd_thd.argtypes = [vp] * 5 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_bwd_thd.restype = i32
     L.te_attn_bwd_thd.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_bwd_thd_ev.restype = i32
+    L.te_attn_bwd_thd_ev.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp, vp]
     L.te_attn_bwd_thd_noalloc.restype = i32
     L.te_attn_bwd_thd_noalloc.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp]
     L.te_attn_read_status.restype = i32
@@ -148,8 +150,11 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv
 
 def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
         cu_seqlens_kv_padded, attn_scale, mask_type="padding", max_seqlen_q=0,
-        max_seqlen_kv=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """``te_attn_bwd_thd``: returns ``(dq, dk, dv)`` in q's dtype."""
+        max_seqlen_kv=0, dq=None, dk=None, dv=None, workspace=None, stream=None,
+        dq_done=None):
+    """``te_attn_bwd_thd``: returns ``(dq, dk, dv)`` in q's dtype. With ``dq_done``
+    (a ``torch.cuda.Event``) it calls ``te_attn_bwd_thd_ev`` instead, which records
+    that event on the stream as soon as dq is final (before dk/dv are computed)."""
     L = library()
     _need_cuda(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                cu_seqlens_kv_padded, dq, dk, dv, workspace)
@@ -168,12 +173,18 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    rc = L.te_attn_bwd_thd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
-        _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
-        _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
-        d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace),
-        workspace.numel(), ctypes.c_void_p(st))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
+            _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+            d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace),
+            workspace.numel(), ctypes.c_void_p(st))
+    if dq_done is None:
+        rc = L.te_attn_bwd_thd(*args)
+    else:
+        if dq_done.cuda_event == 0:  # torch creates the CUDA event on its first record
+            dq_done.record(torch.cuda.ExternalStream(st) if stream is not None
+                           else torch.cuda.current_stream(q.device))
+        rc = L.te_attn_bwd_thd_ev(*args, ctypes.c_void_p(dq_done.cuda_event))
     _check(rc)
     return dq, dk, dv
 

@@ -263,12 +263,13 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   return ok_status();
 }
 
-int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+static int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
                     const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
                     const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
                     int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
-                    int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+                    int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                    cudaEvent_t dq_done) {
   (void)max_seqlen_q;
   (void)max_seqlen_kv;
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
@@ -312,19 +313,51 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
   const bool bf16 = dtype == TE_DTYPE_BF16;
   cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, reinterpret_cast<int*>(ws + L.pref_f), st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  // Rows no tile writes are zeroed first (they depend on the lengths only), so dq
+  // is final as soon as the dQ kernel ends and dk/dv when the dK/dV kernel does.
+  e = timed(TE_KERNEL_ZERO_FILL, st, [&] { return teattn::launch_zero_fill(p, 1, sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "zero fill");
   if (total_q > 0) {
     e = timed(TE_KERNEL_DELTA, st, [&] { return teattn::launch_delta(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "delta");
   }
   if (total_q > 0 && total_kv > 0) {
-    e = timed(TE_KERNEL_DKDV, st, [&] { return teattn::launch_attn_bwd_dkdv(p, bf16, sms, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "dK/dV");
     e = timed(TE_KERNEL_DQ, st, [&] { return teattn::launch_attn_bwd_dq(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "dQ");
   }
-  e = timed(TE_KERNEL_ZERO_FILL, st, [&] { return teattn::launch_zero_fill(p, 1, sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+  if (dq_done) {
+    e = cudaEventRecord(dq_done, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dq event record");
+  }
+  if (total_q > 0 && total_kv > 0) {
+    e = timed(TE_KERNEL_DKDV, st, [&] { return teattn::launch_attn_bwd_dkdv(p, bf16, sms, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "dK/dV");
+  }
   return ok_status();
+}
+
+int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                    const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
+                    int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                    int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, max_seqlen_q, max_seqlen_kv, hq, hkv,
+                  d, attn_scale, mask_type, dtype, workspace, workspace_bytes, stream, nullptr);
+}
+
+int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                       const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
+                       int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                       int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                       void* dq_done) {
+  return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, max_seqlen_q, max_seqlen_kv, hq, hkv,
+                  d, attn_scale, mask_type, dtype, workspace, workspace_bytes, stream,
+                  static_cast<cudaEvent_t>(dq_done));
 }
 
 int te_attn_read_status(const void* workspace, int* status, void* stream) {

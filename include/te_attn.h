@@ -132,6 +132,23 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
                     void* stream);
 
 /*
+ * Backward with a hand-over point (no counterpart in the pages): identical results
+ * to te_attn_bwd_thd, plus `dq_done`, a cudaEvent_t created by the caller (or NULL),
+ * is recorded on `stream` as soon as dq is final -- the backward computes dq before
+ * dk and dv -- so that the caller can start consuming dq (a copy to the host, a
+ * collective) on another stream while dk/dv are still being computed. Returns what
+ * te_attn_bwd_thd returns, or TE_ERR_CUDA if the event cannot be recorded.
+ */
+int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                       const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                       int batch, int total_q, int total_kv, int max_seqlen_q,
+                       int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                       int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                       void* stream, void* dq_done);
+
+/*
  * Synchronises `stream`, then copies the device status word of the last call that
  * used `workspace` into *status (0 = clean, else TE_STATUS_* bits). Returns TE_OK or
  * TE_ERR_CUDA. Intended for tests and debugging; it blocks the host.

@@ -300,3 +300,27 @@ def test_issue3333_reference_norms_from_page_rng():
     bad = [r for r in results if r[1] <= 256 and not r[4]]
     assert not bad, f"page norms not reproduced: {bad} (all: {results})"
     print("issue 3333 norms (lengths, tokens, oracle, page, reproduced):", results)
+
+
+def test_bwd_dq_event_handover():
+    """te_attn_bwd_thd_ev: the same bits as te_attn_bwd_thd, and dq copied on a second
+    stream as soon as the recorded event fires already equals the final dq (the
+    backward computes dq before dk/dv)."""
+    import bwd_packed_varlen_gb300 as ta
+
+    w = W.random_varlen(11, batch=6, max_len=700, hq=8, hkv=2, d=128, mask_type=W.MASK_PADDING_CAUSAL)
+    t = to_dev(w)
+    cu = (t["cu_q"], t["cu_kv"], t["cu_q_pad"], t["cu_kv_pad"])
+    args = (w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv)
+    out, lse = ta.fwd(t["q"], t["k"], t["v"], *cu, *args)
+    ref = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, *args)
+    ev = torch.cuda.Event()
+    side = torch.cuda.Stream()
+    got = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, *args, dq_done=ev)
+    side.wait_event(ev)
+    with torch.cuda.stream(side):
+        early_dq = got[0].clone()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    assert torch.equal(early_dq, got[0])
