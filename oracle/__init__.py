@@ -16,7 +16,9 @@ packed-sequence attention) fix:
 * GQA maps query head h to key/value head h // (hq // hkv) ([3216],
   ``fp32_reference`` with ``repeat_interleave``);
 * the causal mask is the upper-left triangle, key j visible to query i iff j <= i
-  ([3216], ``torch.triu(..., 1)`` filled with -inf);
+  ([3216], ``torch.triu(..., 1)`` filled with -inf); the lower-right variant
+  (``padding_causal_bottom_right``, j <= i + Lk - Lq) is this package's own
+  restatement of that mask name, pinned against torch's ``causal_lower_right``;
 * rows that hold no token of any sequence get exactly-zero gradients ([2448],
   "Expected behavior": the first 4 tokens of dk/dv are zero when the first query
   sequence is empty).
@@ -34,6 +36,8 @@ Pages cited, by title (keys are the pages' issue numbers):
 from .attention import (  # noqa: F401
     MASK_PADDING,
     MASK_PADDING_CAUSAL,
+    MASK_PADDING_CAUSAL_BOTTOM_RIGHT,
+    causal_diagonal,
     seq_spans,
     attn_group_fwd_bwd,
     attn_group_bwd_given,

@@ -18,11 +18,17 @@ Notation follows the TransformerEngine pages this oracle restates:
   the softmax denominator of the *scaled* scores.
 * ``padding_causal`` keeps key j for query i iff ``j <= i`` (upper-left alignment,
   [3216] ``torch.triu(ones, 1)`` masked to -inf).
+* ``padding_causal_bottom_right`` keeps key j for query i iff ``j <= i + Lk - Lq``:
+  the causal triangle aligned to the last query and the last key. The pages use
+  only equal lengths, where the two alignments agree; this variant is the mask
+  name TransformerEngine gives the lower-right alignment, restated from its
+  definition (query i sits at absolute position ``Lk - Lq + i``).
 
 Readings where the pages are silent:
 
-* A valid query whose sequence has no valid key gets ``out = 0``, ``lse = -inf`` and
-  ``dq = 0`` (empty-sum convention).
+* A valid query that sees no key (its sequence has no valid key, or the
+  bottom-right triangle leaves it none when ``Lq > Lk``) gets ``out = 0``,
+  ``lse = -inf`` and ``dq = 0`` (empty-sum convention).
 * Every row that is not a real token (pad slots, tails, rows of empty sequences) is
   exactly 0 in ``out, dq`` and ``lse``; key/value rows that are not real tokens, or
   that no valid query sees, are exactly 0 in ``dk, dv``.
@@ -43,15 +49,24 @@ import numpy as np
 
 MASK_PADDING = 1
 MASK_PADDING_CAUSAL = 2
+MASK_PADDING_CAUSAL_BOTTOM_RIGHT = 3
 
-_MASKS = {MASK_PADDING: False, MASK_PADDING_CAUSAL: True,
-          "padding": False, "padding_causal": True}
+# mask type -> causal alignment: None (no triangle), "tl" (upper-left), "br" (lower-right)
+_MASKS = {MASK_PADDING: None, MASK_PADDING_CAUSAL: "tl", MASK_PADDING_CAUSAL_BOTTOM_RIGHT: "br",
+          "padding": None, "padding_causal": "tl", "padding_causal_bottom_right": "br"}
 
 
-def _is_causal(mask_type) -> bool:
+def _is_causal(mask_type):
+    """Causal alignment of a mask type: None, ``"tl"`` or ``"br"``."""
     if mask_type not in _MASKS:
         raise ValueError(f"unknown mask_type {mask_type!r}")
     return _MASKS[mask_type]
+
+
+def causal_diagonal(causal, lq, lk):
+    """Offset c of the causal boundary: query i keeps key j iff ``j <= i + c``
+    (0 for the upper-left triangle, ``Lk - Lq`` for the lower-right one)."""
+    return lk - lq if causal == "br" else 0
 
 
 def seq_spans(cu_seqlens, cu_seqlens_padded):
@@ -73,8 +88,23 @@ def _scores(qh, kg, scale, causal):
     s = scale * (qh @ kg.T)
     if causal:
         lq, lk = s.shape
-        s[np.arange(lk)[None, :] > np.arange(lq)[:, None]] = -np.inf
+        c = causal_diagonal(causal, lq, lk)
+        s[np.arange(lk)[None, :] > np.arange(lq)[:, None] + c] = -np.inf
     return s
+
+
+def _softmax_rows(s):
+    """``(P, lse)`` of score rows; a row without any kept key gets P = 0 and
+    lse = -inf (empty-sum convention)."""
+    m = s.max(axis=1)
+    seen = np.isfinite(m)
+    ms = np.where(seen, m, 0.0)
+    e = np.where(seen[:, None], np.exp(s - ms[:, None]), 0.0)
+    l = e.sum(axis=1)
+    p = np.divide(e, l[:, None], out=np.zeros_like(e), where=seen[:, None])
+    with np.errstate(divide="ignore"):
+        lse = np.where(seen, ms + np.log(np.where(seen, l, 1.0)), -np.inf)
+    return p, lse
 
 
 def attn_group_fwd_bwd(qg, kg, vg, dog, scale, causal):
@@ -109,11 +139,7 @@ def attn_group_fwd_bwd(qg, kg, vg, dog, scale, causal):
         return out, lse, dq, dk, dv
     for j in range(G):
         s = _scores(qg[:, j, :], kg, scale, causal)
-        m = s.max(axis=1)
-        e = np.exp(s - m[:, None])
-        l = e.sum(axis=1)
-        p = e / l[:, None]
-        lse[:, j] = m + np.log(l)
+        p, lse[:, j] = _softmax_rows(s)
         out[:, j, :] = p @ vg
         do = dog[:, j, :]
         dv += p.T @ do
@@ -150,7 +176,9 @@ def attn_group_bwd_given(qg, kg, vg, outg, dog, lseg, scale, causal):
         return dq, dk, dv
     for j in range(G):
         s = _scores(qg[:, j, :], kg, scale, causal)
-        p = np.exp(s - lseg[:, j][:, None])
+        # a row without kept keys contributes nothing (its lse is -inf)
+        keep = np.isfinite(s)
+        p = np.where(keep, np.exp(np.where(keep, s, 0.0) - np.where(keep, lseg[:, j][:, None], 0.0)), 0.0)
         do = dog[:, j, :]
         dv += p.T @ do
         dp = do @ vg.T
@@ -255,10 +283,11 @@ def valid_row_masks(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                     cu_seqlens_kv_padded, T_q, T_kv, mask_type):
     """Which rows may be nonzero: ``(q_rows [T_q], kv_rows [T_kv])`` booleans.
 
-    A query row may be nonzero iff it is a real token of a sequence with at least
-    one real key; a key/value row may be nonzero in dk/dv iff it is a real token that
-    some real query sees (padding: the sequence has a query; padding_causal: also
-    its index is below the query length, since query i sees keys j <= i).
+    A query row may be nonzero iff it is a real token that sees at least one real
+    key; a key/value row may be nonzero in dk/dv iff it is a real token that some
+    real query sees (padding: the sequence has a query; padding_causal: also its
+    index is below the query length, since query i sees keys j <= i;
+    padding_causal_bottom_right: every real key, since the last query sees all).
     Every other row must be exactly 0 ([2448] "Expected behavior").
     Parity: pinned by the golden fixtures of [2448] and [2892].
     """
@@ -269,10 +298,12 @@ def valid_row_masks(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
     km = np.zeros(T_kv, dtype=bool)
     for (oq, lq), (ok, lk) in zip(qs, ks):
         if lk > 0:
-            qm[oq:oq + lq] = True
+            # query i sees key 0 iff 0 <= i + c
+            first = max(0, -causal_diagonal(causal, lq, lk)) if causal else 0
+            qm[oq + min(first, lq):oq + lq] = True
         if lq > 0:
-            seen = min(lk, lq) if causal else lk
-            km[ok:ok + seen] = True
+            seen = min(lk, lq + causal_diagonal(causal, lq, lk)) if causal else lk
+            km[ok:ok + max(seen, 0)] = True
     return qm, km
 
 
@@ -280,7 +311,7 @@ def fwd_bwd_flops(cu_seqlens_q, cu_seqlens_kv, hq, d, mask_type):
     """Causal-adjusted algorithmic FLOPs of forward + backward (test helper).
 
     Per (sequence, query head): ``F_fwd = 4 d pairs`` with ``pairs = Lq Lk``
-    (padding) or ``Lq Lk / 2`` (padding_causal); forward + backward is ``3.5 F_fwd``
+    (padding) or ``Lq Lk / 2`` (either causal alignment); forward + backward is ``3.5 F_fwd``
     (2 GEMMs forward, 5 backward)."""
     causal = _is_causal(mask_type)
     lq = np.diff(np.asarray(cu_seqlens_q, dtype=np.int64)).astype(np.float64)

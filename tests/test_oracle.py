@@ -20,7 +20,11 @@ import pytest
 import torch
 
 import oracle
-from oracle import MASK_PADDING, MASK_PADDING_CAUSAL
+from oracle import MASK_PADDING, MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT
+
+ALL_MASKS = [MASK_PADDING, MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT]
+# torch's own constructions of the two causal alignments
+_ALIGN = {MASK_PADDING: None, MASK_PADDING_CAUSAL: "tl", MASK_PADDING_CAUSAL_BOTTOM_RIGHT: "br"}
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -45,7 +49,7 @@ def _loss(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, mask):
     return float((out * do).sum())
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+@pytest.mark.parametrize("mask", ALL_MASKS)
 def test_finite_differences(mask):
     """Central differences of L = sum(dO * O) w.r.t. every element of q, k, v agree
     with the oracle's dq, dk, dv (float64, eps 1e-6), including the exact-zero
@@ -76,7 +80,9 @@ def test_finite_differences(mask):
 
 def _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, causal):
     """Per-sequence torch float64 SDPA (math) + autograd with repeat_interleave GQA,
-    the reference construction of [3333] and [3216]."""
+    the reference construction of [3333] and [3216]. ``causal``: None, "tl" (a
+    lower-triangular boolean mask) or "br" (torch's ``causal_lower_right`` bias,
+    whose fully masked rows torch's math backend returns as zeros)."""
     hq, hkv = q.shape[1], k.shape[1]
     G = hq // hkv
     tq = torch.tensor(q, requires_grad=True)
@@ -93,11 +99,18 @@ def _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, causal):
         qi = tq[oq:oq + Lq].transpose(0, 1)
         ki = tk[ok:ok + Lk].transpose(0, 1).repeat_interleave(G, 0)
         vi = tv[ok:ok + Lk].transpose(0, 1).repeat_interleave(G, 0)
-        mask = None
-        if causal:
-            mask = torch.ones(Lq, Lk, dtype=torch.bool).tril()
+        mask = bias = None
+        if causal == "tl":
+            mask = bias = torch.ones(Lq, Lk, dtype=torch.bool).tril()
+        elif causal == "br":
+            import warnings
+            from torch.nn.attention.bias import causal_lower_right
+            with warnings.catch_warnings():
+                warnings.simplefilter("ignore")  # it warns about rows with no key
+                bias = causal_lower_right(Lq, Lk)
+            mask = bias._materialize(device=qi.device)
         o = torch.nn.functional.scaled_dot_product_attention(
-            qi, ki, vi, attn_mask=mask, scale=scale)
+            qi, ki, vi, attn_mask=bias, scale=scale)
         s = scale * qi @ ki.transpose(-1, -2)
         if causal:
             s = s.masked_fill(~mask, float("-inf"))
@@ -113,7 +126,7 @@ def _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, causal):
             tv.grad.numpy())
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+@pytest.mark.parametrize("mask", ALL_MASKS)
 @pytest.mark.parametrize("seed", [2, 3])
 def test_matches_torch_sdpa_autograd(mask, seed):
     """Oracle == torch.nn.functional.scaled_dot_product_attention (float64, CPU) +
@@ -123,9 +136,12 @@ def test_matches_torch_sdpa_autograd(mask, seed):
     q, k, v, do, cu_q, cu_k, cp_q, cp_k = _rand_case(seed, lq, lk, pq, pk, 4, 2, 16)
     scale = 0.25
     mine = oracle.attn_fwd_bwd_thd(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, mask)
-    ref = _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale,
-                           mask == MASK_PADDING_CAUSAL)
+    ref = _torch_reference(q, k, v, do, cu_q, cu_k, cp_q, cp_k, scale, _ALIGN[mask])
     for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), mine, ref):
+        # rows that see no key: -inf in both lse (lower-right, Lq > Lk)
+        inf = np.isneginf(b)
+        assert np.array_equal(np.isneginf(a), inf), name
+        a, b = np.where(inf, 0.0, a), np.where(inf, 0.0, b)
         assert np.abs(a - b).max() <= 1e-10 * max(1.0, np.abs(b).max()), name
     given = oracle.attn_bwd_thd(q, k, v, mine[0], do, mine[1], cu_q, cu_k, cp_q, cp_k,
                                 scale, mask)
@@ -208,7 +224,83 @@ def test_causal_first_row_and_zero_query():
     assert np.allclose(lse, math.log(6.0), atol=1e-14)
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+def test_bottom_right_closed_forms():
+    """Lower-right causal alignment: with Lq == Lk it is the upper-left triangle,
+    bit for bit; a single query (Lq = 1) sees every key, as with the padding mask;
+    with Lk = 1 only the last query sees the key (O = V_0, LSE = scale q.k_0) and
+    the Lq - 1 queries before it see nothing (O = 0, LSE = -inf, dQ = 0)."""
+    br, tl = MASK_PADDING_CAUSAL_BOTTOM_RIGHT, MASK_PADDING_CAUSAL
+    args = _rand_case(21, [6, 4], [6, 4], [7, 4], [6, 5], 2, 1, 5)
+    a = oracle.attn_fwd_bwd_thd(*args, 0.5, br)
+    b = oracle.attn_fwd_bwd_thd(*args, 0.5, tl)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    args = _rand_case(22, [1], [7], [2], [9], 3, 1, 4)
+    a = oracle.attn_fwd_bwd_thd(*args, 0.5, br)
+    b = oracle.attn_fwd_bwd_thd(*args, 0.5, MASK_PADDING)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    q, k, v, do, cu_q, cu_k, cp_q, cp_k = _rand_case(23, [5], [1], [6], [3], 3, 1, 4)
+    out, lse, dq, dk, dv = oracle.attn_fwd_bwd_thd(q, k, v, do, cu_q, cu_k, cp_q, cp_k,
+                                                   0.3, br)
+    assert np.all(out[:4] == 0) and np.all(dq[:4] == 0) and np.all(np.isneginf(lse[:4]))
+    assert np.allclose(out[4], np.broadcast_to(v[0, 0], (3, 4)), atol=1e-14)
+    assert np.allclose(lse[4], 0.3 * q[4] @ k[0, 0], atol=1e-13)
+    assert np.abs(dq[4]).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    assert np.allclose(dv[0, 0], do[4].sum(axis=0), atol=1e-12)
+
+
+@pytest.mark.parametrize("lq,lk", [(3, 8), (5, 5), (8, 3), (1, 4), (4, 1)])
+def test_bottom_right_is_shifted_top_left(lq, lk):
+    """The lower-right triangle puts query i at position Lk - Lq + i. So for
+    Lq <= Lk it is the upper-left problem over Lk queries of which only the last
+    Lq carry a gradient (the others get dO = 0 and change nothing in dK/dV); for
+    Lq > Lk the last Lk queries form the upper-left problem and the first Lq - Lk
+    see no key. Checked on out, lse, dq, dk, dv against the upper-left oracle."""
+    br, tl = MASK_PADDING_CAUSAL_BOTTOM_RIGHT, MASK_PADDING_CAUSAL
+    q, k, v, do, _, _, _, _ = _rand_case(30 + lq * 10 + lk, [lq], [lk], [lq], [lk], 4, 2, 6, tail=0)
+    cq, ck = [0, lq], [0, lk]
+    out, lse, dq, dk, dv = oracle.attn_fwd_bwd_thd(q, k, v, do, cq, ck, cq, ck, 0.45, br)
+    if lq <= lk:
+        rng = np.random.default_rng(lq + 100 * lk)
+        qx = np.concatenate([rng.standard_normal((lk - lq,) + q.shape[1:]), q])
+        dox = np.concatenate([np.zeros((lk - lq,) + q.shape[1:]), do])
+        c = [0, lk]
+        o2, l2, dq2, dk2, dv2 = oracle.attn_fwd_bwd_thd(qx, k, v, dox, c, c, c, c, 0.45, tl)
+        sl = slice(lk - lq, lk)
+        pairs = ((out, o2[sl]), (lse, l2[sl]), (dq, dq2[sl]), (dk, dk2), (dv, dv2))
+    else:
+        c = [0, lk]
+        o2, l2, dq2, dk2, dv2 = oracle.attn_fwd_bwd_thd(q[lq - lk:], k, v, do[lq - lk:], c, c,
+                                                        c, c, 0.45, tl)
+        n = lq - lk
+        assert np.all(out[:n] == 0) and np.all(dq[:n] == 0) and np.all(np.isneginf(lse[:n]))
+        pairs = ((out[n:], o2), (lse[n:], l2), (dq[n:], dq2), (dk, dk2), (dv, dv2))
+    for a, b in pairs:
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_bottom_right_zero_rows():
+    """Lower-right alignment with more queries than keys: the leading queries that
+    see no key are exactly 0 in out and dq with lse -inf, and every real key row is
+    seen (the last query sees them all)."""
+    lq, lk, pq, pk = [7, 2, 3], [3, 5, 0], [8, 4, 3], [4, 5, 2]
+    q, k, v, do, cu_q, cu_k, cp_q, cp_k = _rand_case(24, lq, lk, pq, pk, 2, 2, 4, tail=1)
+    br = MASK_PADDING_CAUSAL_BOTTOM_RIGHT
+    out, lse, dq, dk, dv = oracle.attn_fwd_bwd_thd(q, k, v, do, cu_q, cu_k, cp_q, cp_k, 0.5, br)
+    qm, km = oracle.valid_row_masks(cu_q, cu_k, cp_q, cp_k, q.shape[0], k.shape[0], br)
+    # sequence 0: queries 0-3 see no key; sequence 2 has no key at all
+    assert list(np.nonzero(qm)[0]) == [4, 5, 6, 8, 9]
+    assert list(np.nonzero(km)[0]) == [0, 1, 2, 4, 5, 6, 7, 8]
+    assert np.all(out[~qm] == 0) and np.all(dq[~qm] == 0)
+    assert np.all(np.abs(out[qm]).sum(axis=(1, 2)) > 0)
+    assert np.all(dk[~km] == 0) and np.all(dv[~km] == 0)
+    assert np.all(np.abs(dv[km]).sum(axis=(1, 2)) > 0)
+    assert np.all(np.isneginf(lse[[0, 1, 2, 3, 12, 13, 14]]))
+    assert np.all(lse[[7, 10, 11, 15]] == 0)
+
+
+@pytest.mark.parametrize("mask", ALL_MASKS)
 def test_invariants(mask):
     """Softmax rows sum to 1 (O = 1 for V = 1); LSE = logsumexp of the scaled,
     masked scores (scipy); sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per sequence
@@ -217,7 +309,7 @@ def test_invariants(mask):
     lq, lk, pq, pk = [6, 9, 4], [6, 9, 7], [8, 9, 4], [6, 12, 7]
     q, k, v, do, cu_q, cu_k, cp_q, cp_k = _rand_case(6, lq, lk, pq, pk, 4, 2, 8)
     scale = 0.4
-    causal = mask == MASK_PADDING_CAUSAL
+    causal = _ALIGN[mask]
     out1, _ = oracle.attn_fwd_thd(q, k, np.ones_like(v), cu_q, cu_k, cp_q, cp_k, scale, mask)
     qm, _ = oracle.valid_row_masks(cu_q, cu_k, cp_q, cp_k, q.shape[0], k.shape[0], mask)
     assert np.allclose(out1[qm], 1.0, atol=1e-14)
@@ -231,7 +323,9 @@ def test_invariants(mask):
             for h in range(g * G, g * G + G):
                 s = scale * q[oq:oq + Lq, h] @ kk.T
                 if causal:
-                    s = np.where(np.tril(np.ones((Lq, Lk), dtype=bool)), s, -np.inf)
+                    # query i sits at position i (upper-left) or Lk - Lq + i (lower-right)
+                    pos = np.arange(Lq) + (Lk - Lq if causal == "br" else 0)
+                    s = np.where(np.arange(Lk)[None, :] <= pos[:, None], s, -np.inf)
                 assert np.allclose(lse[oq:oq + Lq, h], logsumexp(s, axis=1), atol=1e-12)
             assert np.abs(dk[ok:ok + Lk, g].sum(axis=0)).max() < 1e-11
             rows = slice(oq, oq + Lq)
@@ -242,7 +336,7 @@ def test_invariants(mask):
             assert lhs == pytest.approx(rhs, rel=1e-11, abs=1e-11)
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+@pytest.mark.parametrize("mask", ALL_MASKS)
 def test_gqa_identity(mask):
     """GQA dK/dV equal the MHA gradients with K/V repeat_interleaved over each
     group and summed back over the group; out/lse/dq are unchanged."""
@@ -259,7 +353,7 @@ def test_gqa_identity(mask):
         assert np.allclose(a, summed, atol=1e-12)
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+@pytest.mark.parametrize("mask", ALL_MASKS)
 def test_packed_equals_unpacked(mask):
     """THD packing with padded offsets gives, row for row, what each sequence gives
     on its own (offset 0, no padding, batch of 1); pad-slot contents are ignored."""
@@ -293,7 +387,7 @@ def test_packed_equals_unpacked(mask):
         assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("mask", [MASK_PADDING, MASK_PADDING_CAUSAL])
+@pytest.mark.parametrize("mask", ALL_MASKS)
 def test_exact_zero_rows(mask):
     """Pad slots, tail rows, empty sequences and key rows no query sees are exactly
     zero in out/lse/dq/dk/dv; rows that may be nonzero are nonzero here."""
