@@ -9,6 +9,7 @@ CUDA device.
 from ._binding import (  # noqa: F401
     MASK_PADDING,
     MASK_PADDING_CAUSAL,
+    MASK_PADDING_CAUSAL_BOTTOM_RIGHT,
     TeAttnError,
     bwd,
     bwd_noalloc,
@@ -22,4 +23,9 @@ from ._binding import (  # noqa: F401
     library_path,
     read_status,
     version,
+)
+from .autograd import (  # noqa: F401
+    DotProductAttention,
+    THDAttentionFunction,
+    dot_product_attention,
 )

@@ -15,7 +15,9 @@ import torch
 
 MASK_PADDING = 1
 MASK_PADDING_CAUSAL = 2
-_MASK_NAMES = {"padding": MASK_PADDING, "padding_causal": MASK_PADDING_CAUSAL}
+MASK_PADDING_CAUSAL_BOTTOM_RIGHT = 3
+_MASK_NAMES = {"padding": MASK_PADDING, "padding_causal": MASK_PADDING_CAUSAL,
+               "padding_causal_bottom_right": MASK_PADDING_CAUSAL_BOTTOM_RIGHT}
 _DTYPES = {torch.float16: 0, torch.bfloat16: 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

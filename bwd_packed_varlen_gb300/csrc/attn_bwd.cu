@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     it.kt = pr.y;
     it.b = pr.x;
     it.s = load_seq(p, pr.x);
-    it.qt0 = causal ? (it.kt * kBlockN) / kBM : 0;
+    it.qt0 = first_query(it.s, it.kt * kBlockN, causal) / kBM;
     it.nq = (it.s.len_q + kBM - 1) / kBM;
     it.steps = p.group * (it.nq - it.qt0);
     return it;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // query columns i of this warp with a nonzero P^T for this key row: [lo, hi)
         const int q_base = qt * kBM + col0;
         const int hi = kv_valid ? min(kG, I.s.len_q - q_base) : 0;
-        const int lo = causal ? max(0, kv_row - q_base) : 0;
+        const int lo = causal ? max(0, kv_row - I.s.diag - q_base) : 0;
         // Warp-uniform: only tiles on the causal diagonal or a length boundary pay
         // for per-element masking.
         const bool full = __all_sync(0xffffffffu, lo == 0 && hi >= kG);
@@ -550,15 +550,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       int nxt = blockIdx.x;
       for (; ok; ++ii) {
-        const int item = nxt < n_items ? nxt : -1;
+        int item = nxt < n_items ? nxt : -1;
+        int2 pr;
+        SeqInfo s;
+        int n = 0;
+        // Query tiles that see no key (rows before a lower-right causal triangle)
+        // are left to the zero fill and never reach the ring.
+        while (item >= 0) {
+          pr = p.q_pairs[item / p.hq];
+          s = load_seq(p, pr.x);
+          n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
+          if (n > 0) break;
+          nxt = next_item(p.header + kHdrNextDq);
+          item = nxt < n_items ? nxt : -1;
+        }
         if (item < 0) {
           ok = ring_put(ring, ii, -1, status);
           break;
         }
-        const int2 pr = p.q_pairs[item / p.hq];
         const int h = item % p.hq, g = h / p.group;
-        const SeqInfo s = load_seq(p, pr.x);
-        const int n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
         // the step count travels with the item: the MMA thread then needs no global loads
         if (!(ok = ring_put(ring, ii, item, status, n))) break;
         nxt = next_item(p.header + kHdrNextDq);  // used at the next hand-over
@@ -674,12 +684,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SeqInfo s = load_seq(p, pr.x);
       r.n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
       const int row = pr.y * kBlockM + quarter * 32 + lane;
-      r.row_valid = row < s.len_q;
+      // rows that see no key (before a lower-right triangle) are the zero fill's
+      r.lim = row < s.len_q ? row_keys(s, row, causal) : 0;
+      r.row_valid = r.lim > 0;
       r.gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
       const size_t ti = tiled_index(p, pr.x, row, h);
       r.lse2 = r.row_valid ? p.lse_t[ti] : 0.f;
       r.dlt = r.row_valid ? p.delta_t[ti] : 0.f;
-      r.lim = r.row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
       return r;
     };
     int it = 0, ii = 0;

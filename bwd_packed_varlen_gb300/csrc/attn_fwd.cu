@@ -111,13 +111,17 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmV);
       int it = 0, ii = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int2 pr = p.q_pairs[item / p.hq];
         const int h = item % p.hq, g = h / p.group;
         const SeqInfo s = load_seq(p, pr.x);
         const int qt = pr.y;
         const int n = (visible_keys(s, qt, causal) + kBlockN - 1) / kBlockN;
-        if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
+        // a tile that sees no key (before a lower-right causal triangle) is the
+        // zero fill's; every role skips it without touching a barrier
+        if (n == 0) continue;
+        const int k = ii++;  // index of this item among the block's processed ones
+        if (k > 0 && !(ok = mbar_wait(&bar_q_empty, (k - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_q_full, S::kTileBytes);
         for (int c = 0; c < S::kChunks; ++c)
           tma_load_3d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.off_q + qt * kBlockM);
@@ -163,11 +167,13 @@ __global__ void __launch_bounds__(192, 1)
         mma_commit(&bar_k_empty[sk]);
         return true;
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++ii) {
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int2 pr = p.q_pairs[item / p.hq];
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBlockN - 1) / kBlockN;
-        if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
+        if (n == 0) continue;
+        const int k = ii++;  // index of this item among the block's processed ones
+        if (!(ok = mbar_wait(&bar_q_full, k & 1, status))) break;
         if (!(ok = issue_s(it))) break;
         for (int j = 0; j < n && ok; ++j) {
           const int cur = it + j;
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
           if (!(ok = mbar_wait(&bar_p_ready[cur & 1], (cur >> 1) & 1, status))) break;
           const int sv = cur % SV;
           if (!(ok = mbar_wait(&bar_v_full[sv], (cur / SV) & 1, status))) break;
-          if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_o_empty, (ii - 1) & 1, status))) break;
+          if (j == 0 && k > 0 && !(ok = mbar_wait(&bar_o_empty, (k - 1) & 1, status))) break;
           tc_fence_after();
           const uint32_t a_tmem = tmem + S::kColS0 + (cur & 1) * kBlockN;
           const SmemDesc vst{dv.lo + ((sv * S::kTileBytes) >> 4), dv.hi};
@@ -205,9 +211,11 @@ __global__ void __launch_bounds__(192, 1)
       const SeqInfo s = load_seq(p, pr.x);
       const int qt = pr.y;
       const int n = (visible_keys(s, qt, causal) + kBlockN - 1) / kBlockN;
+      if (n == 0) continue;
       const int row = qt * kBlockM + tid;
-      const bool row_valid = row < s.len_q;
-      const int lim = row_valid ? (causal ? min(s.len_k, row + 1) : s.len_k) : 0;
+      // rows that see no key (before a lower-right triangle) are the zero fill's
+      const int lim = row < s.len_q ? row_keys(s, row, causal) : 0;
+      const bool row_valid = lim > 0;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const int cur = it + j;

@@ -136,12 +136,20 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       bool ok = true;
       int nxt = blockIdx.x;
       for (; ok; ++ii) {
-        const int item = nxt < n_items ? nxt : -1;
+        int item = nxt < n_items ? nxt : -1;
+        FwdItem I;
+        // Items whose two tiles see no key (rows before a lower-right causal
+        // triangle) are left to the zero fill and never reach the ring.
+        while (item >= 0) {
+          I = fwd_item(p, item, causal);
+          if (I.nmax > 0) break;
+          nxt = next_item(p.header + kHdrNextFwd);
+          item = nxt < n_items ? nxt : -1;
+        }
         if (item < 0) {
           ok = ring_put(ring, ii, -1, status);
           break;
         }
-        const FwdItem I = fwd_item(p, item, causal);
         // both tiles' key-tile counts travel with the item: the MMA thread then
         // needs no global loads (which would queue behind the softmax warps' O stores)
         if (!(ok = ring_put(ring, ii, item, status, I.n[0] | (I.n[1] << 16)))) break;
@@ -276,8 +284,9 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       const FwdItem I = fwd_item(p, item, causal);
       r.n = I.n[x];
       const int row = (2 * I.u + x) * kBlockM + quarter * 32 + lane;
-      r.row_valid = row < I.s.len_q;
-      r.lim = r.row_valid ? (causal ? min(I.s.len_k, row + 1) : I.s.len_k) : 0;
+      // rows that see no key (before a lower-right triangle) are the zero fill's
+      r.lim = row < I.s.len_q ? row_keys(I.s, row, causal) : 0;
+      r.row_valid = r.lim > 0;
       r.out_row = static_cast<size_t>(I.s.off_q + row) * p.hq + I.h;
       return r;
     };

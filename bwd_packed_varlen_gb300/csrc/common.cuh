@@ -63,7 +63,7 @@ struct AttnParams {
   int hkv;
   int d;
   int group;         // hq / hkv
-  int causal;        // 1 for padding_causal
+  int causal;        // 0 padding; 1 causal, upper-left; 2 causal, lower-right
   float scale;       // attn_scale
   float scale_log2;  // attn_scale * log2(e)
 
@@ -82,6 +82,7 @@ struct AttnParams {
 // inconsistent; the scheduler flags those in the status word.
 struct SeqInfo {
   int off_q, len_q, off_k, len_k;
+  int diag;  // causal boundary: query i sees key j iff j <= i + diag
   bool ok;
 };
 
@@ -101,6 +102,9 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
     s.len_q = 0;
     s.len_k = 0;
   }
+  // Upper-left alignment puts query i at key position i; lower-right puts it at
+  // len_k - len_q + i, so the last query sees every key.
+  s.diag = p.causal == 2 ? s.len_k - s.len_q : 0;
   return s;
 }
 
@@ -111,17 +115,29 @@ __device__ __forceinline__ size_t tiled_index(const AttnParams& p, int b, int i,
   return (static_cast<size_t>(pair) * p.hq + h) * kBlockM + (i % kBlockM);
 }
 
-// Number of key rows a query tile can see (upper-left causal: key j <= query i).
+// Number of keys (a prefix 0 .. n-1) that real query row i sees: all of them
+// without the causal mask, keys j <= i + diag with it. Zero for a query before
+// the lower-right triangle starts.
+__device__ __forceinline__ int row_keys(const SeqInfo& s, int i, bool causal) {
+  return causal ? min(s.len_k, max(0, i + 1 + s.diag)) : s.len_k;
+}
+
+// Number of key rows a query tile can see (the keys its last real row sees).
 __device__ __forceinline__ int visible_keys(const SeqInfo& s, int q_tile, bool causal) {
   if (!causal) return s.len_k;
-  int last_q = min((q_tile + 1) * kBlockM, s.len_q);  // exclusive
-  return min(s.len_k, last_q);
+  const int last_q = min((q_tile + 1) * kBlockM, s.len_q);  // exclusive
+  return min(s.len_k, max(0, last_q + s.diag));
+}
+
+// First query row that sees key j (causal: i >= j - diag).
+__device__ __forceinline__ int first_query(const SeqInfo& s, int j, bool causal) {
+  return causal ? max(0, j - s.diag) : 0;
 }
 
 // Number of key rows some real query sees (the rest get exact-zero dk/dv).
 __device__ __forceinline__ int seen_keys(const SeqInfo& s, bool causal) {
   if (s.len_q == 0) return 0;
-  return causal ? min(s.len_k, s.len_q) : s.len_k;
+  return causal ? min(s.len_k, max(0, s.len_q + s.diag)) : s.len_k;
 }
 
 }  // namespace teattn

@@ -19,8 +19,10 @@ namespace teattn {
 //   k pairs  (sequence, key tile)              -- dK/dV items (x hkv heads)
 //   f pairs  (sequence, pair of query tiles)   -- forward items (x hq heads)
 // Tiles cover the REAL length of each sequence; sequences without a real query
-// or key produce no pair, and key tiles no real query sees (causal, beyond the
-// query length) produce none either -- those rows are zero-filled instead.
+// or key produce no pair, and key tiles no real query sees (upper-left causal,
+// beyond the query length) produce none either -- those rows are zero-filled
+// instead. Query tiles whose rows all precede a lower-right causal triangle are
+// listed but see no key: the kernels skip them and the zero fill writes them.
 // Each list is sorted by estimated cost (key tiles the item visits), largest
 // first, ties by natural order, so a persistent grid takes the long items first.
 // Up to kSortCap pairs are sorted in shared memory; a longer list keeps its
@@ -72,7 +74,7 @@ __device__ int q_pair_cost(const AttnParams& p, int b, int t) {
 __device__ int k_pair_cost(const AttnParams& p, int b, int t) {
   SeqInfo s = load_seq(p, b);
   int nq = (s.len_q + kBlockM - 1) / kBlockM;
-  return p.causal ? nq - (t * kBlockN) / kBlockM : nq;
+  return nq - first_query(s, t * kBlockN, p.causal) / kBlockM;
 }
 
 // Forward item of two query tiles: both tiles' key tiles (the second sees most).
@@ -222,13 +224,15 @@ __device__ __forceinline__ int seq_of_row(const int* cu_pad, int B, int r) {
   return lo;
 }
 
-// 0: not computed; 1: computed by a tensor-core kernel; 2: real query without keys.
+// 0: not computed; 1: computed by a tensor-core kernel; 2: real query that sees
+// no key (its sequence has none, or the lower-right triangle starts after it).
 __device__ __forceinline__ int q_row_kind(const AttnParams& p, int r) {
   int b = seq_of_row(p.cu_q_pad, p.batch, r);
   if (b < 0) return 0;
   SeqInfo s = load_seq(p, b);
-  if (r - s.off_q >= s.len_q) return 0;
-  return s.len_k > 0 ? 1 : 2;
+  const int i = r - s.off_q;
+  if (i >= s.len_q) return 0;
+  return row_keys(s, i, p.causal) > 0 ? 1 : 2;
 }
 
 __device__ __forceinline__ bool k_row_computed(const AttnParams& p, int r) {

@@ -112,8 +112,11 @@ int check_common(int batch, int total_q, int total_kv, int hq, int hkv, int d, f
   if (hq % hkv != 0) return fail(TE_ERR_INVALID_ARG, "hq must be a multiple of hkv");
   if (d < 8 || d > 256 || d % 8 != 0)
     return fail(TE_ERR_UNSUPPORTED, "head dim must be a multiple of 8 in [8, 256]");
-  if (mask_type != TE_MASK_PADDING && mask_type != TE_MASK_PADDING_CAUSAL)
-    return fail(TE_ERR_UNSUPPORTED, "mask_type must be TE_MASK_PADDING or TE_MASK_PADDING_CAUSAL");
+  if (mask_type != TE_MASK_PADDING && mask_type != TE_MASK_PADDING_CAUSAL &&
+      mask_type != TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT)
+    return fail(TE_ERR_UNSUPPORTED,
+                "mask_type must be TE_MASK_PADDING, TE_MASK_PADDING_CAUSAL or "
+                "TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT");
   if (dtype != TE_DTYPE_FP16 && dtype != TE_DTYPE_BF16)
     return fail(TE_ERR_UNSUPPORTED, "dtype must be TE_DTYPE_FP16 or TE_DTYPE_BF16");
   if (!std::isfinite(attn_scale)) return fail(TE_ERR_INVALID_ARG, "attn_scale must be finite");
@@ -139,7 +142,8 @@ teattn::AttnParams base_params(const int32_t* cu_q, const int32_t* cu_kv, const 
   p.hkv = hkv;
   p.d = d;
   p.group = hq / hkv;
-  p.causal = mask_type == TE_MASK_PADDING_CAUSAL ? 1 : 0;
+  p.causal = mask_type == TE_MASK_PADDING_CAUSAL ? 1
+             : mask_type == TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT ? 2 : 0;
   p.scale = attn_scale;
   p.scale_log2 = attn_scale * 1.4426950408889634f;
   char* ws = static_cast<char*>(workspace);

@@ -36,6 +36,7 @@ import torch
 
 MASK_PADDING = 1
 MASK_PADDING_CAUSAL = 2
+MASK_PADDING_CAUSAL_BOTTOM_RIGHT = 3
 
 _DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
 
@@ -82,10 +83,11 @@ class Workload:
 
     def algorithmic_flops(self) -> float:
         """Causal-adjusted fwd+bwd FLOPs: per (sequence, query head)
-        ``3.5 * 4 * d * pairs``, pairs = Lq*Lk (padding) or Lq*Lk/2 (causal)."""
+        ``3.5 * 4 * d * pairs``, pairs = Lq*Lk (padding) or Lq*Lk/2 (either causal
+        alignment)."""
         lq = (self.cu_seqlens_q[1:] - self.cu_seqlens_q[:-1]).double()
         lk = (self.cu_seqlens_kv[1:] - self.cu_seqlens_kv[:-1]).double()
-        f = 0.5 if self.mask_type == MASK_PADDING_CAUSAL else 1.0
+        f = 0.5 if self.mask_type in (MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT) else 1.0
         return float(3.5 * 4.0 * self.d * self.hq * (lq * lk * f).sum().item())
 
 

@@ -34,13 +34,18 @@
  *       tokens are the first (cu_*[b+1]-cu_*[b]) of those rows.
  *   Rows that are not real tokens (pad slots, tails after cu_*_padded[batch], rows
  *   of empty sequences) are written as exact zeros in out/dq/dk/dv and 0 in lse;
- *   key/value rows no real query sees are exact zeros in dk/dv. A real query of a
- *   sequence with no real key gets out = 0, lse = -inf, dq = 0.
+ *   key/value rows no real query sees are exact zeros in dk/dv. A real query that
+ *   sees no key (its sequence has no real key, or it precedes a lower-right
+ *   causal triangle) gets out = 0, lse = -inf, dq = 0.
  *   Pad slots may hold any finite values; they never reach a real output.
  *
  * Supported: d a multiple of 8 with 8 <= d <= 256; hq a positive multiple of hkv;
- *   mask TE_MASK_PADDING or TE_MASK_PADDING_CAUSAL (key j visible to query i iff
- *   j <= i, upper-left aligned); dtype TE_DTYPE_FP16 or TE_DTYPE_BF16.
+ *   mask TE_MASK_PADDING, TE_MASK_PADDING_CAUSAL (key j visible to query i iff
+ *   j <= i, upper-left aligned, the alignment [3216] uses) or
+ *   TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT (key j visible iff j <= i + Lk - Lq, the
+ *   triangle aligned to the last query and key; TransformerEngine's
+ *   "padding_causal_bottom_right" -- the pages use equal lengths only, where the
+ *   two causal masks agree); dtype TE_DTYPE_FP16 or TE_DTYPE_BF16.
  *
  * Determinism: no floating-point atomics; every output element is produced by one
  *   thread block in a fixed order, so repeated calls on identical inputs give
@@ -75,6 +80,7 @@ extern "C" {
 
 #define TE_MASK_PADDING 1
 #define TE_MASK_PADDING_CAUSAL 2
+#define TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT 3
 
 #define TE_DTYPE_FP16 0
 #define TE_DTYPE_BF16 1

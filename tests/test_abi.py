@@ -74,3 +74,26 @@ def test_binding_signatures_match_header(lib):
     for name, n in counts.items():
         fn = getattr(lib, name)
         assert fn.argtypes is not None and len(fn.argtypes) == n, (name, n, fn.argtypes)
+
+
+def test_autograd_wrapper_has_no_cpu_path():
+    """The DotProductAttention-like wrapper refuses CPU tensors and unsupported
+    layouts before any compute; the mask aliases map to the C ABI's three masks."""
+    import torch
+    import bwd_packed_varlen_gb300 as ta
+    from bwd_packed_varlen_gb300 import autograd as ag
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        ta.dot_product_attention(q, kv, kv, cu, cu)
+    with pytest.raises(ValueError):
+        ta.DotProductAttention(2, 64, 1)(q, kv, kv, cu, cu)
+    with pytest.raises(NotImplementedError):
+        ta.dot_product_attention(q, kv, kv, cu, cu, qkv_format="sbhd")
+    with pytest.raises(ValueError):
+        ta.DotProductAttention(3, 64, 2)
+    assert {ag._mask_name(m) for m in ("causal", "padding_causal")} == {"padding_causal"}
+    assert ag._mask_name("causal_bottom_right") == "padding_causal_bottom_right"
+    assert ag._mask_name("no_mask") == "padding"
+    assert ta._binding._mask("padding_causal_bottom_right") == 3

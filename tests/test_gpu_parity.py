@@ -122,6 +122,10 @@ EDGE = [
     (19, 6, 129, 8, 2, 32, W.MASK_PADDING_CAUSAL, "bf16"),
     (20, 4, 400, 8, 8, 16, W.MASK_PADDING_CAUSAL, "bf16"),
     (21, 3, 400, 4, 2, 192, W.MASK_PADDING_CAUSAL, "bf16"),
+    (22, 6, 500, 4, 2, 64, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, "bf16"),
+    (23, 5, 400, 6, 3, 128, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, "fp16"),
+    (24, 3, 400, 4, 1, 256, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, "bf16"),
+    (25, 4, 300, 4, 4, 48, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, "bf16"),
 ]
 
 
@@ -132,6 +136,55 @@ def test_ragged_edge_cases(case):
     seed, batch, max_len, hq, hkv, d, mask, dtype = case
     w = W.random_varlen(seed, batch, max_len, hq, hkv, d, mask, dtype)
     check_against_oracle(w, gpu_fwd_bwd(w))
+
+
+def _same_bits(x, y):
+    view = torch.int32 if x.dtype == torch.float32 else torch.int16
+    return torch.equal(x.view(view), y.view(view))
+
+
+def _lengths_case(lq, lk, hq, hkv, d, mask, seed, pad=9):
+    """THD workload with the given real query/key lengths per sequence."""
+    import math
+    rng = np.random.default_rng(seed)
+    lq, lk = np.asarray(lq), np.asarray(lk)
+    pq = lq + rng.integers(0, pad + 1, size=lq.size)
+    pk = lk + rng.integers(0, pad + 1, size=lk.size)
+    cu = lambda x: torch.tensor([0] + list(np.cumsum(x)), dtype=torch.int32)
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda T, h: torch.randn(T, h, d, generator=g).to(torch.bfloat16)
+    Tq, Tk = int(pq.sum()) + 3, int(pk.sum()) + 3
+    return W.Workload(name=f"lengths_{seed}", q=mk(Tq, hq), k=mk(Tk, hkv), v=mk(Tk, hkv),
+                      dout=mk(Tq, hq), cu_seqlens_q=cu(lq), cu_seqlens_kv=cu(lk),
+                      cu_seqlens_q_padded=cu(pq), cu_seqlens_kv_padded=cu(pk),
+                      attn_scale=1.0 / math.sqrt(d), mask_type=mask, dtype="bf16")
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_bottom_right_causal(d):
+    """Lower-right causal alignment: more queries than keys (whole query tiles and
+    forward tile pairs before the triangle see no key: out 0, lse -inf, dq 0),
+    fewer queries than keys (every key row seen), equal lengths (bit-identical to
+    the upper-left mask), bit-identical on a repeated call."""
+    lq, lk = [700, 130, 384, 1, 300], [150, 900, 384, 77, 0]
+    w = _lengths_case(lq, lk, 4, 2, d, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, 50 + d)
+    t = to_dev(w)
+    a = gpu_fwd_bwd(w, t)
+    check_against_oracle(w, a)
+    b = gpu_fwd_bwd(w, t)
+    for x, y in zip(a, b):
+        assert _same_bits(x, y)
+    # first sequence: queries 0..549 see no key
+    o0 = int(w.cu_seqlens_q_padded[0])
+    assert torch.all(a[0][o0:o0 + 550] == 0) and torch.all(a[2][o0:o0 + 550] == 0)
+    assert torch.all(torch.isneginf(a[1][o0:o0 + 550]))
+    eq = _lengths_case([384, 200], [384, 200], 4, 2, d, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT, 60 + d)
+    te = to_dev(eq)
+    br = gpu_fwd_bwd(eq, te)
+    eq.mask_type = W.MASK_PADDING_CAUSAL
+    tl = gpu_fwd_bwd(eq, te)
+    for x, y in zip(br, tl):
+        assert _same_bits(x, y)
 
 
 def test_all_sequences_empty_and_keyless():
@@ -205,7 +258,7 @@ def test_invalid_arguments_return_errors():
                t["v"][..., :12].contiguous(), *cu, 0.1, 1)
     assert e.value.code == -2
     with pytest.raises(ta.TeAttnError) as e:
-        ta.fwd(t["q"], t["k"], t["v"], *cu, 0.1, 3)
+        ta.fwd(t["q"], t["k"], t["v"], *cu, 0.1, 4)
     assert e.value.code == -2
     with pytest.raises(ta.TeAttnError) as e:
         ta.fwd(t["q"], t["k"], t["v"], *cu, 0.1, 1,
