@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     bwd,
     bwd_noalloc,
     fwd,
+    fwd_sbhd,
+    bwd_sbhd,
     fwd_workspace_size,
     KERNELS,
     profile_enable,
@@ -26,6 +28,7 @@ from ._binding import (  # noqa: F401
 )
 from .autograd import (  # noqa: F401
     DotProductAttention,
+    SBHDAttentionFunction,
     THDAttentionFunction,
     dot_product_attention,
 )

@@ -62,6 +62,10 @@ def library() -> ctypes.CDLL:
     L.te_attn_bwd_thd_ev.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp, vp]
     L.te_attn_bwd_thd_noalloc.restype = i32
     L.te_attn_bwd_thd_noalloc.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp]
+    L.te_attn_fwd_sbhd.restype = i32
+    L.te_attn_fwd_sbhd.argtypes = [vp] * 5 + [vp] * 2 + [i32] * 6 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_bwd_sbhd.restype = i32
+    L.te_attn_bwd_sbhd.argtypes = [vp] * 9 + [vp] * 2 + [i32] * 6 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_read_status.restype = i32
     L.te_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     L.te_attn_last_error.restype = ctypes.c_char_p
@@ -188,6 +192,60 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
                            else torch.cuda.current_stream(q.device))
         rc = L.te_attn_bwd_thd_ev(*args, ctypes.c_void_p(dq_done.cuda_event))
     _check(rc)
+    return dq, dk, dv
+
+
+def fwd_sbhd(q, k, v, cu_seqlens_q, cu_seqlens_kv, attn_scale, mask_type="padding", out=None,
+             lse=None, workspace=None, stream=None):
+    """``te_attn_fwd_sbhd``: q ``[S_q, B, hq, d]``, k/v ``[S_kv, B, hkv, d]``, real
+    lengths from ``cu_seqlens_q/kv``; returns ``(out [S_q, B, hq, d], lse [S_q, B, hq])``."""
+    L = library()
+    _need_cuda(q, k, v, cu_seqlens_q, cu_seqlens_kv, out, lse, workspace)
+    _cu(cu_seqlens_q, cu_seqlens_kv)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    Sq, B, hq, d = q.shape
+    Sk, Bk, hkv, _ = k.shape
+    if Bk != B or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v must be [S, B, h, d] with one batch size; v shaped like k")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Sq, B, hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = fwd_workspace_size(B, Sq * B, Sk * B, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    _check(L.te_attn_fwd_sbhd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+        B, Sq, Sk, hq, hkv, d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype],
+        _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
+    return out, lse
+
+
+def bwd_sbhd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, attn_scale,
+             mask_type="padding", dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """``te_attn_bwd_sbhd``: returns ``(dq, dk, dv)`` in the shapes of q, k, v."""
+    L = library()
+    _need_cuda(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, dq, dk, dv, workspace)
+    _cu(cu_seqlens_q, cu_seqlens_kv)
+    if q.dtype not in _DTYPES or any(t.dtype != q.dtype for t in (k, v, out, dout)):
+        raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    Sq, B, hq, d = q.shape
+    Sk, Bk, hkv, _ = k.shape
+    if Bk != B or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v must be [S, B, h, d] with one batch size; v shaped like k")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_size(B, Sq * B, Sk * B, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    _check(L.te_attn_bwd_sbhd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Sq, Sk, hq, hkv, d, float(attn_scale),
+        _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
     return dq, dk, dv
 
 

@@ -18,12 +18,13 @@ Readings where the pages are silent:
 * ``attn_mask_type`` ``"causal"`` / ``"no_mask"`` / ``"causal_bottom_right"`` mean
   their ``padding_*`` forms: with packed input the real lengths always mask.
 * ``qkv_format="bshd"`` (``[B, S, h, d]``, contiguous) is the packed layout with
-  padded offsets ``b * S``; no data moves. ``"sbhd"`` is not supported (its
-  sequences interleave token by token, which the kernels' row addressing does not
-  express) and raises.
+  padded offsets ``b * S``; no data moves. ``"sbhd"`` (``[S, B, h, d]``, the
+  layout of [3216]) runs on the library's sequence-major entry points. In both,
+  ``cu_seqlens_q/kv`` are optional real lengths (default: all S tokens).
 
 Pages cited, by title (keys are the pages' issue numbers):
   [2448] "Inconsistent fused_attn_bwd results of dk, dv under THD layout + GQA on multiple calls"
+  [3216] "flash-attn-4 4.0.0b11: DotProductAttention batched backward returns wrong dQ/dK/dV at head_dim=256 on Blackwell (sm_100)"
   [2892] "[BUG] SIGSEGV in fused_attn_fwd when cu_seqlens_q != cu_seqlens_q_padded with FP8 blockwise"
 """
 
@@ -55,8 +56,8 @@ class THDAttentionFunction(torch.autograd.Function):
     """``out = attention(q, k, v)`` over packed sequences with a fused backward.
 
     ``q [T_q, hq, d]``, ``k, v [T_kv, hkv, d]`` contiguous CUDA tensors; returns
-    ``out [T_q, hq, d]``. The backward returns ``dq, dk, dv`` (GQA dk/dv summed
-    over each head group) and no gradient for the index tensors."""
+    ``(out [T_q, hq, d], lse [T_q, hq])``. The backward returns ``dq, dk, dv`` (GQA
+    dk/dv summed over each head group) and no gradient for the index tensors."""
 
     @staticmethod
     def forward(ctx, q, k, v, cu_q, cu_kv, cu_q_pad, cu_kv_pad, scale, mask, max_q, max_kv):
@@ -77,10 +78,35 @@ class THDAttentionFunction(torch.autograd.Function):
         return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
+class SBHDAttentionFunction(torch.autograd.Function):
+    """The same over the sequence-major layout: ``q [S_q, B, hq, d]``, ``k, v
+    [S_kv, B, hkv, d]``, real lengths ``cu_q, cu_kv``; returns ``(out, lse [S_q, B,
+    hq])``."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, cu_q, cu_kv, scale, mask):
+        out, lse = _b.fwd_sbhd(q, k, v, cu_q, cu_kv, scale, mask)
+        ctx.save_for_backward(q, k, v, out, lse, cu_q, cu_kv)
+        ctx.args = (scale, mask)
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, _dlse):
+        q, k, v, out, lse, cu_q, cu_kv = ctx.saved_tensors
+        scale, mask = ctx.args
+        dq, dk, dv = _b.bwd_sbhd(q, k, v, out, dout.contiguous(), lse, cu_q, cu_kv, scale, mask)
+        return dq, dk, dv, None, None, None, None
+
+
+def _full_lengths(B, S, device):
+    return torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=device)
+
+
 def _bshd_to_thd(x, cu_real, S):
     # a view, never a copy: a non-contiguous input fails here instead of moving data
     B = x.shape[0]
-    cu_pad = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=x.device)
+    cu_pad = _full_lengths(B, S, x.device)
     if cu_real is None:
         cu_real = cu_pad
     return x.view(B * S, x.shape[2], x.shape[3]), cu_real, cu_pad
@@ -94,9 +120,11 @@ def dot_product_attention(q, k, v, cu_seqlens_q=None, cu_seqlens_kv=None,
 
     ``thd``: ``q [T_q, hq, d]``, ``k, v [T_kv, hkv, d]``; ``cu_seqlens_q/kv`` (int32
     ``[B+1]``) are required and the padded ones default to them. ``bshd``: ``q [B,
-    S_q, hq, d]``, ``k, v [B, S_kv, hkv, d]``; ``cu_seqlens_*`` are optional real
-    lengths (default: full). ``softmax_scale`` defaults to ``1 / sqrt(d)``. Returns
-    ``[T_q, hq * d]`` (``[B, S_q, hq * d]`` for bshd), plus ``lse [T_q, hq]`` when
+    S_q, hq, d]``, ``k, v [B, S_kv, hkv, d]``; ``sbhd``: ``q [S_q, B, hq, d]``, ``k, v
+    [S_kv, B, hkv, d]``; for both, ``cu_seqlens_*`` are optional real lengths
+    (default: full). ``softmax_scale`` defaults to ``1 / sqrt(d)``. Returns ``[T_q,
+    hq * d]`` (``[B, S_q, hq * d]`` for bshd, ``[S_q, B, hq * d]`` for sbhd), plus
+    the fp32 lse (``[T_q, hq]``, ``[B * S_q, hq]``, ``[S_q, B, hq]``) when
     ``return_lse``."""
     mask = _mask_name(attn_mask_type)
     if qkv_format == "bshd":
@@ -112,6 +140,18 @@ def dot_product_attention(q, k, v, cu_seqlens_q=None, cu_seqlens_kv=None,
         k3, cu_kv, cu_kv_pad = _bshd_to_thd(k, cu_seqlens_kv, Sk)
         v3 = v.view(Bq * Sk, v.shape[2], v.shape[3])
         shape = (Bq, Sq, q.shape[2] * q.shape[3])
+    elif qkv_format == "sbhd":
+        if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+            raise ValueError("sbhd tensors must be [S, B, h, d]")
+        if cu_seqlens_q_padded is not None or cu_seqlens_kv_padded is not None:
+            raise ValueError("sbhd takes no padded cu_seqlens: every entry spans S tokens")
+        Sq, B = q.shape[:2]
+        cu_q = _full_lengths(B, Sq, q.device) if cu_seqlens_q is None else cu_seqlens_q
+        cu_kv = _full_lengths(B, k.shape[0], q.device) if cu_seqlens_kv is None else cu_seqlens_kv
+        scale = 1.0 / math.sqrt(q.shape[-1]) if softmax_scale is None else float(softmax_scale)
+        out, lse = SBHDAttentionFunction.apply(q, k, v, cu_q, cu_kv, scale, mask)
+        out = out.view(Sq, B, q.shape[2] * q.shape[3])
+        return (out, lse) if return_lse else out
     elif qkv_format == "thd":
         if cu_seqlens_q is None or cu_seqlens_kv is None:
             raise ValueError("thd needs cu_seqlens_q and cu_seqlens_kv")
@@ -121,7 +161,7 @@ def dot_product_attention(q, k, v, cu_seqlens_q=None, cu_seqlens_kv=None,
         cu_kv_pad = cu_seqlens_kv if cu_seqlens_kv_padded is None else cu_seqlens_kv_padded
         shape = (q.shape[0], q.shape[1] * q.shape[2])
     else:
-        raise NotImplementedError(f"qkv_format {qkv_format!r}: only 'thd' and 'bshd'")
+        raise NotImplementedError(f"qkv_format {qkv_format!r}: 'thd', 'bshd' or 'sbhd'")
     scale = 1.0 / math.sqrt(q.shape[-1]) if softmax_scale is None else float(softmax_scale)
     out, lse = THDAttentionFunction.apply(q3, k3, v3, cu_q, cu_kv, cu_q_pad, cu_kv_pad, scale,
                                           mask, int(max_seqlen_q or 0), int(max_seqlen_kv or 0))

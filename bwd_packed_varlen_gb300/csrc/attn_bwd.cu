@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ii > 0 && !(ok = mbar_wait(&bar_kv_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_kv_full, 2 * S::kKVBytes);
         for (int c = 0; c < S::kChunks; ++c) {
-          tma_load_3d(sK + c * 16384, &tmK, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
-          tma_load_3d(sV + c * 16384, &tmV, &bar_kv_full, c * 64, I.g, I.s.off_k + I.kt * kBlockN);
+          tma_load_4d(sK + c * 16384, &tmK, &bar_kv_full, c * 64, I.g, I.s.tb, I.s.off_k + I.kt * kBlockN);
+          tma_load_4d(sV + c * 16384, &tmV, &bar_kv_full, c * 64, I.g, I.s.tb, I.s.off_k + I.kt * kBlockN);
         }
         const int nqt = I.nq - I.qt0;
         for (int t = 0; t < I.steps; ++t, ++it) {
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (it >= NS && !(ok = mbar_wait(&bar_q_empty[st], ((it / NS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_q_full[st], 2 * S::kQBytes + 2 * kBM * 4);
           for (int c = 0; c < S::kChunks; ++c) {
-            tma_load_3d(sQ + st * S::kQBytes + c * kBM * 128, &tmQ, &bar_q_full[st], c * 64, h,
+            tma_load_4d(sQ + st * S::kQBytes + c * kBM * 128, &tmQ, &bar_q_full[st], c * 64, h, I.s.tb,
                         I.s.off_q + qt * kBM);
-            tma_load_3d(sDO + st * S::kQBytes + c * kBM * 128, &tmDO, &bar_q_full[st], c * 64, h,
+            tma_load_4d(sDO + st * S::kQBytes + c * kBM * 128, &tmDO, &bar_q_full[st], c * 64, h, I.s.tb,
                         I.s.off_q + qt * kBM);
           }
           const size_t ti = tiled_index(p, I.b, qt * kBM, h);
@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int kv_row = I.kt * kBlockN + quarter * 32 + lane;
       const bool kv_valid = kv_row < I.s.len_k;
       const int nqt = I.nq - I.qt0;
+      // tensor row of key token 0: the loop carries one value for the epilogue
+      const int kv_row0 = I.s.off_k * p.rs + I.s.tb;
       for (int t = 0; t < I.steps; ++t, ++it) {
         const int qt = I.qt0 + t % nqt;
         const int st = it % NS;
@@ -416,7 +418,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool store = kv_row < seen_keys(I.s, causal);
-      const size_t kv_off = (static_cast<size_t>(I.s.off_k + kv_row) * p.hkv + I.g) * p.d;
+      const size_t kv_off =
+          ((static_cast<size_t>(kv_row0) + static_cast<size_t>(kv_row) * p.rs) * p.hkv + I.g) * p.d;
       const auto dk_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dk) + kv_off, store);
       const auto dv_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dv) + kv_off, store);
       const int col_out = I.split * S::kDo;
@@ -575,20 +578,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_q_full, 2 * S::kQBytes);
         for (int c = 0; c < S::kChunks; ++c) {
-          tma_load_3d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.off_q + pr.y * kBlockM);
-          tma_load_3d(sDO + c * 16384, &tmDO, &bar_q_full, c * 64, h, s.off_q + pr.y * kBlockM);
+          tma_load_4d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.tb, s.off_q + pr.y * kBlockM);
+          tma_load_4d(sDO + c * 16384, &tmDO, &bar_q_full, c * 64, h, s.tb, s.off_q + pr.y * kBlockM);
         }
         for (int j = 0; j < n; ++j, ++it) {
           const int sk = it % KS, sv = it % VS;
           if (it >= KS && !(ok = mbar_wait(&bar_k_empty[sk], ((it / KS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_k_full[sk], S::kKVBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sK + sk * S::kKVBytes + c * kBN * 128, &tmK, &bar_k_full[sk], c * 64, g,
+            tma_load_4d(sK + sk * S::kKVBytes + c * kBN * 128, &tmK, &bar_k_full[sk], c * 64, g, s.tb,
                         s.off_k + j * kBN);
           if (it >= VS && !(ok = mbar_wait(&bar_v_empty[sv], ((it / VS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_v_full[sv], S::kKVBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sV + sv * S::kKVBytes + c * kBN * 128, &tmV, &bar_v_full[sv], c * 64, g,
+            tma_load_4d(sV + sv * S::kKVBytes + c * kBN * 128, &tmV, &bar_v_full[sv], c * 64, g, s.tb,
                         s.off_k + j * kBN);
         }
       }
@@ -687,7 +690,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // rows that see no key (before a lower-right triangle) are the zero fill's
       r.lim = row < s.len_q ? row_keys(s, row, causal) : 0;
       r.row_valid = r.lim > 0;
-      r.gi = static_cast<size_t>(s.off_q + row) * p.hq + h;
+      r.gi = q_row(p, s, row) * p.hq + h;
       const size_t ti = tiled_index(p, pr.x, row, h);
       r.lse2 = r.row_valid ? p.lse_t[ti] : 0.f;
       r.dlt = r.row_valid ? p.delta_t[ti] : 0.f;
@@ -801,10 +804,11 @@ template <int kD, bool kBF16>
 static cudaError_t launch_dkdv_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
   using S = DkdvShape<kD>;
   CUtensorMap tq, tdo, tk, tv;
-  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16, S::kBM) ||
-      !make_tmap_thd(&tdo, p.dout, p.total_q, p.hq, p.d, kBF16, S::kBM) ||
-      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16, 128) ||
-      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16, 128))
+  const int nb = p.sbhd ? p.batch : 1;
+  if (!make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16, S::kBM) ||
+      !make_tmap_tokens(&tdo, p.dout, p.total_q, nb, p.hq, p.d, kBF16, S::kBM) ||
+      !make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16, 128) ||
+      !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16, 128))
     return cudaErrorInvalidValue;
   auto kern = attn_bwd_dkdv_kernel<kD, kBF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
@@ -819,10 +823,11 @@ template <int kD, bool kBF16>
 static cudaError_t launch_dq_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
   using S = DqShape<kD>;
   CUtensorMap tq, tdo, tk, tv;
-  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16, 128) ||
-      !make_tmap_thd(&tdo, p.dout, p.total_q, p.hq, p.d, kBF16, 128) ||
-      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16, S::kBN) ||
-      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16, S::kBN))
+  const int nb = p.sbhd ? p.batch : 1;
+  if (!make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16, 128) ||
+      !make_tmap_tokens(&tdo, p.dout, p.total_q, nb, p.hq, p.d, kBF16, 128) ||
+      !make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16, S::kBN) ||
+      !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16, S::kBN))
     return cudaErrorInvalidValue;
   auto kern = attn_bwd_dq_kernel<kD, kBF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);

@@ -124,19 +124,19 @@ __global__ void __launch_bounds__(192, 1)
         if (k > 0 && !(ok = mbar_wait(&bar_q_empty, (k - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&bar_q_full, S::kTileBytes);
         for (int c = 0; c < S::kChunks; ++c)
-          tma_load_3d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.off_q + qt * kBlockM);
+          tma_load_4d(sQ + c * 16384, &tmQ, &bar_q_full, c * 64, h, s.tb, s.off_q + qt * kBlockM);
         for (int j = 0; j < n; ++j, ++it) {
           const int sk = it % SK;
           if (it >= SK && !(ok = mbar_wait(&bar_k_empty[sk], ((it / SK) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_k_full[sk], S::kTileBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sK + sk * S::kTileBytes + c * 16384, &tmK, &bar_k_full[sk], c * 64, g,
+            tma_load_4d(sK + sk * S::kTileBytes + c * 16384, &tmK, &bar_k_full[sk], c * 64, g, s.tb,
                         s.off_k + j * kBlockN);
           const int sv = it % SV;
           if (it >= SV && !(ok = mbar_wait(&bar_v_empty[sv], ((it / SV) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_v_full[sv], S::kTileBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sV + sv * S::kTileBytes + c * 16384, &tmV, &bar_v_full[sv], c * 64, g,
+            tma_load_4d(sV + sv * S::kTileBytes + c * 16384, &tmV, &bar_v_full[sv], c * 64, g, s.tb,
                         s.off_k + j * kBlockN);
         }
       }
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(192, 1)
       const float inv = l > 0.f ? 1.0f / l : 0.f;
       using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
       T* orow = static_cast<T*>(p.out) +
-                (static_cast<size_t>(s.off_q + row) * p.hq + h) * static_cast<size_t>(p.d);
+                (q_row(p, s, row) * p.hq + h) * static_cast<size_t>(p.d);
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t o[32];
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (row_valid)
-        p.lse[static_cast<size_t>(s.off_q + row) * p.hq + h] = m * 0.69314718055994531f + logf(l);
+        p.lse[q_row(p, s, row) * p.hq + h] = m * 0.69314718055994531f + logf(l);
       tc_fence_before();
       mbar_arrive(&bar_o_empty);
       it += n;
@@ -363,9 +363,10 @@ static cudaError_t launch_fwd_impl(const AttnParams& p, int num_sms, cudaStream_
   using S = FwdShape<kD>;
   CUtensorMap tq, tk, tv;
   const bool bf16 = kBF16;
-  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, bf16) ||
-      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, bf16) ||
-      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, bf16))
+  const int nb = p.sbhd ? p.batch : 1;
+  if (!make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, bf16) ||
+      !make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, bf16) ||
+      !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, bf16))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_kernel<kD, kBF16>;
   cudaError_t e =

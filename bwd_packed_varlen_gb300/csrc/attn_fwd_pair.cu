@@ -159,19 +159,19 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         mbar_arrive_expect_tx(&bar_q_full, ntiles * S::kTileBytes);
         for (int x = 0; x < ntiles; ++x)
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sQ + x * S::kTileBytes + c * 16384, &tmQ, &bar_q_full, c * 64, I.h,
+            tma_load_4d(sQ + x * S::kTileBytes + c * 16384, &tmQ, &bar_q_full, c * 64, I.h, I.s.tb,
                         I.s.off_q + (2 * I.u + x) * kBlockM);
         for (int j = 0; j < I.nmax; ++j, ++it) {
           const int st = it % NS;
           if (it >= NS && !(ok = mbar_wait(&bar_k_empty[st], ((it / NS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_k_full[st], S::kTileBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sK + st * S::kTileBytes + c * 16384, &tmK, &bar_k_full[st], c * 64, I.g,
+            tma_load_4d(sK + st * S::kTileBytes + c * 16384, &tmK, &bar_k_full[st], c * 64, I.g, I.s.tb,
                         I.s.off_k + j * kBlockN);
           if (it >= NS && !(ok = mbar_wait(&bar_v_empty[st], ((it / NS) - 1) & 1, status))) break;
           mbar_arrive_expect_tx(&bar_v_full[st], S::kTileBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_3d(sV + st * S::kTileBytes + c * 16384, &tmV, &bar_v_full[st], c * 64, I.g,
+            tma_load_4d(sV + st * S::kTileBytes + c * 16384, &tmV, &bar_v_full[st], c * 64, I.g, I.s.tb,
                         I.s.off_k + j * kBlockN);
         }
       }
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       // rows that see no key (before a lower-right triangle) are the zero fill's
       r.lim = row < I.s.len_q ? row_keys(I.s, row, causal) : 0;
       r.row_valid = r.lim > 0;
-      r.out_row = static_cast<size_t>(I.s.off_q + row) * p.hq + I.h;
+      r.out_row = q_row(p, I.s, row) * p.hq + I.h;
       return r;
     };
     RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));
@@ -425,9 +425,10 @@ template <int kD, bool kBF16>
 static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
   using S = FwdPairShape<kD>;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_thd(&tq, p.q, p.total_q, p.hq, p.d, kBF16) ||
-      !make_tmap_thd(&tk, p.k, p.total_kv, p.hkv, p.d, kBF16) ||
-      !make_tmap_thd(&tv, p.v, p.total_kv, p.hkv, p.d, kBF16))
+  const int nb = p.sbhd ? p.batch : 1;
+  if (!make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16) ||
+      !make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16) ||
+      !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_pair_kernel<kD, kBF16>;
   cudaError_t e =

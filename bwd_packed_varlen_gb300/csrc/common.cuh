@@ -63,6 +63,9 @@ struct AttnParams {
   int hkv;
   int d;
   int group;         // hq / hkv
+  int sbhd;          // 0: packed rows (token i of sequence b at row cu_*_padded[b] + i);
+                     // 1: sequence-major (token i of sequence b at row i * batch + b)
+  int rs;            // rows between consecutive tokens of a sequence: 1, or batch
   int causal;        // 0 padding; 1 causal, upper-left; 2 causal, lower-right
   float scale;       // attn_scale
   float scale_log2;  // attn_scale * log2(e)
@@ -81,7 +84,8 @@ struct AttnParams {
 // extents. Returns false (length 0) for a sequence whose cu_seqlens are
 // inconsistent; the scheduler flags those in the status word.
 struct SeqInfo {
-  int off_q, len_q, off_k, len_k;
+  int off_q, len_q, off_k, len_k;  // off: token coordinate of token 0 in the tensor maps
+  int tb;    // batch coordinate in the tensor maps (0 packed, b sequence-major)
   int diag;  // causal boundary: query i sees key j iff j <= i + diag
   bool ok;
 };
@@ -90,14 +94,24 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
   SeqInfo s;
   int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
   int k0 = p.cu_kv[b], k1 = p.cu_kv[b + 1];
-  int pq0 = p.cu_q_pad[b], pq1 = p.cu_q_pad[b + 1];
-  int pk0 = p.cu_kv_pad[b], pk1 = p.cu_kv_pad[b + 1];
   s.len_q = q1 - q0;
   s.len_k = k1 - k0;
-  s.off_q = pq0;
-  s.off_k = pk0;
-  s.ok = s.len_q >= 0 && s.len_k >= 0 && pq0 >= 0 && pk0 >= 0 && s.len_q <= pq1 - pq0 &&
-         s.len_k <= pk1 - pk0 && pq1 <= p.total_q && pk1 <= p.total_kv;
+  if (p.sbhd) {
+    // every sequence spans the whole token extent of its batch entry
+    s.off_q = 0;
+    s.off_k = 0;
+    s.tb = b;
+    s.ok = s.len_q >= 0 && s.len_k >= 0 && s.len_q <= p.total_q / p.batch &&
+           s.len_k <= p.total_kv / p.batch;
+  } else {
+    int pq0 = p.cu_q_pad[b], pq1 = p.cu_q_pad[b + 1];
+    int pk0 = p.cu_kv_pad[b], pk1 = p.cu_kv_pad[b + 1];
+    s.off_q = pq0;
+    s.off_k = pk0;
+    s.tb = 0;
+    s.ok = s.len_q >= 0 && s.len_k >= 0 && pq0 >= 0 && pk0 >= 0 && s.len_q <= pq1 - pq0 &&
+           s.len_k <= pk1 - pk0 && pq1 <= p.total_q && pk1 <= p.total_kv;
+  }
   if (!s.ok) {
     s.len_q = 0;
     s.len_k = 0;
@@ -106,6 +120,32 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
   // len_k - len_q + i, so the last query sees every key.
   s.diag = p.causal == 2 ? s.len_k - s.len_q : 0;
   return s;
+}
+
+// Tensor rows of query token i / key token j of sequence s (row-major [rows, h, d]).
+__device__ __forceinline__ size_t q_row(const AttnParams& p, const SeqInfo& s, int i) {
+  return static_cast<size_t>(s.off_q + i) * p.rs + s.tb;
+}
+__device__ __forceinline__ size_t k_row(const AttnParams& p, const SeqInfo& s, int j) {
+  return static_cast<size_t>(s.off_k + j) * p.rs + s.tb;
+}
+
+// Sequence holding tensor row r and the token index there (*i); -1 when no
+// sequence's span holds it. cu_pad: the padded prefix sums of the row's tensor.
+__device__ __forceinline__ int locate_row(const AttnParams& p, const int* cu_pad, int r, int* i) {
+  if (p.sbhd) {
+    *i = r / p.batch;
+    return r % p.batch;
+  }
+  const int B = p.batch;
+  if (r < cu_pad[0] || r >= cu_pad[B]) return -1;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_pad[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  *i = r - cu_pad[lo];
+  return lo;
 }
 
 // Index of (natural query-tile pair of row i of sequence b, head h, row in tile)

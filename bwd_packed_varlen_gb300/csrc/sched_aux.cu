@@ -212,34 +212,23 @@ cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, int* 
 // ---------------------------------------------------------------------------
 // Row classification shared by the zero fill and the preprocess
 // ---------------------------------------------------------------------------
-// Sequence b whose padded span holds row r, or -1 (before the first span, after
-// the last, or inconsistent offsets).
-__device__ __forceinline__ int seq_of_row(const int* cu_pad, int B, int r) {
-  if (r < cu_pad[0] || r >= cu_pad[B]) return -1;
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (cu_pad[mid] <= r) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // 0: not computed; 1: computed by a tensor-core kernel; 2: real query that sees
 // no key (its sequence has none, or the lower-right triangle starts after it).
 __device__ __forceinline__ int q_row_kind(const AttnParams& p, int r) {
-  int b = seq_of_row(p.cu_q_pad, p.batch, r);
+  int i = 0;
+  const int b = locate_row(p, p.cu_q_pad, r, &i);
   if (b < 0) return 0;
   SeqInfo s = load_seq(p, b);
-  const int i = r - s.off_q;
   if (i >= s.len_q) return 0;
   return row_keys(s, i, p.causal) > 0 ? 1 : 2;
 }
 
 __device__ __forceinline__ bool k_row_computed(const AttnParams& p, int r) {
-  int b = seq_of_row(p.cu_kv_pad, p.batch, r);
+  int j = 0;
+  const int b = locate_row(p, p.cu_kv_pad, r, &j);
   if (b < 0) return false;
   SeqInfo s = load_seq(p, b);
-  return r - s.off_k < seen_keys(s, p.causal);
+  return j < seen_keys(s, p.causal);
 }
 
 // ---------------------------------------------------------------------------
@@ -311,10 +300,10 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
   const int chunks = p.hq * cpr;
   constexpr float kLog2e = 1.4426950408889634f;
   for (int r = gw; r < p.total_q; r += warps) {
-    const int b = seq_of_row(p.cu_q_pad, p.batch, r);
+    int i = 0;
+    const int b = locate_row(p, p.cu_q_pad, r, &i);
     if (b < 0) continue;
     const SeqInfo s = load_seq(p, b);
-    const int i = r - s.off_q;
     if (i >= s.len_q || s.len_k == 0) continue;  // no tile reads this row
     const size_t row = static_cast<size_t>(r);
     const size_t t0 = tiled_index(p, b, i, 0);   // + h * 128 for head h

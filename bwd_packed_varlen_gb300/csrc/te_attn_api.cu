@@ -142,6 +142,8 @@ teattn::AttnParams base_params(const int32_t* cu_q, const int32_t* cu_kv, const 
   p.hkv = hkv;
   p.d = d;
   p.group = hq / hkv;
+  p.sbhd = 0;
+  p.rs = 1;
   p.causal = mask_type == TE_MASK_PADDING_CAUSAL ? 1
              : mask_type == TE_MASK_PADDING_CAUSAL_BOTTOM_RIGHT ? 2 : 0;
   p.scale = attn_scale;
@@ -213,14 +215,13 @@ size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
   return make_layout(batch, total_q, total_kv, hq, true, &L) ? L.total : 0;
 }
 
-int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, float* lse,
+// Forward of either layout: sbhd = false packs sequences by cu_seqlens_*_padded,
+// sbhd = true puts token i of sequence b at row i * batch + b.
+static int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
                     const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int batch,
-                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int hq, int hkv,
-                    int d, float attn_scale, int mask_type, int dtype, void* workspace,
-                    size_t workspace_bytes, void* stream) {
-  (void)max_seqlen_q;
-  (void)max_seqlen_kv;
+                    int total_q, int total_kv, int hq, int hkv, int d, float attn_scale, int mask_type,
+                    int dtype, void* workspace, size_t workspace_bytes, void* stream, bool sbhd) {
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
                         cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                         workspace);
@@ -241,6 +242,10 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   teattn::AttnParams p = base_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                                      cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d,
                                      attn_scale, mask_type, workspace, L);
+  if (sbhd) {
+    p.sbhd = 1;
+    p.rs = batch;
+  }
   p.q = q;
   p.k = k;
   p.v = v;
@@ -267,15 +272,45 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
   return ok_status();
 }
 
+int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, float* lse,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int batch,
+                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int hq, int hkv,
+                    int d, float attn_scale, int mask_type, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
+  return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
+                  dtype, workspace, workspace_bytes, stream, false);
+}
+
+// Rows of a [seq, batch, heads, d] tensor; -1 (an error) for bad sizes or int overflow.
+static int sbhd_rows(int batch, int seq) {
+  if (batch < 1 || seq < 0) return -1;
+  const long long rows = static_cast<long long>(batch) * seq;
+  return rows > INT32_MAX ? -1 : static_cast<int>(rows);
+}
+
+int te_attn_fwd_sbhd(const void* q, const void* k, const void* v, void* out, float* lse,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch, int seq_q,
+                     int seq_kv, int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  const int tq = sbhd_rows(batch, seq_q), tk = sbhd_rows(batch, seq_kv);
+  if (tq < 0 || tk < 0) return fail(TE_ERR_INVALID_ARG, "batch >= 1, seq_q/seq_kv >= 0, rows < 2^31");
+  // the real prefix sums stand in for the padded ones, which this layout does not use
+  return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q, cu_seqlens_kv,
+                  batch, tq, tk, hq, hkv, d, attn_scale, mask_type, dtype, workspace,
+                  workspace_bytes, stream, true);
+}
+
 static int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
                     const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
                     const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
-                    int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
-                    int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream,
-                    cudaEvent_t dq_done) {
-  (void)max_seqlen_q;
-  (void)max_seqlen_kv;
+                    int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream, cudaEvent_t dq_done,
+                    bool sbhd) {
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
                         cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                         workspace);
@@ -298,6 +333,10 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   teattn::AttnParams p = base_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                                      cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d,
                                      attn_scale, mask_type, workspace, L);
+  if (sbhd) {
+    p.sbhd = 1;
+    p.rs = batch;
+  }
   p.q = q;
   p.k = k;
   p.v = v;
@@ -346,9 +385,11 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
                     const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
                     int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
                     int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
   return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
-                  cu_seqlens_kv_padded, batch, total_q, total_kv, max_seqlen_q, max_seqlen_kv, hq, hkv,
-                  d, attn_scale, mask_type, dtype, workspace, workspace_bytes, stream, nullptr);
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
+                  dtype, workspace, workspace_bytes, stream, nullptr, false);
 }
 
 int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -358,10 +399,23 @@ int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* 
                        int max_seqlen_q, int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
                        int mask_type, int dtype, void* workspace, size_t workspace_bytes, void* stream,
                        void* dq_done) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
   return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
-                  cu_seqlens_kv_padded, batch, total_q, total_kv, max_seqlen_q, max_seqlen_kv, hq, hkv,
-                  d, attn_scale, mask_type, dtype, workspace, workspace_bytes, stream,
-                  static_cast<cudaEvent_t>(dq_done));
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
+                  dtype, workspace, workspace_bytes, stream, static_cast<cudaEvent_t>(dq_done), false);
+}
+
+int te_attn_bwd_sbhd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                     const int32_t* cu_seqlens_kv, int batch, int seq_q, int seq_kv, int hq, int hkv,
+                     int d, float attn_scale, int mask_type, int dtype, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  const int tq = sbhd_rows(batch, seq_q), tk = sbhd_rows(batch, seq_kv);
+  if (tq < 0 || tk < 0) return fail(TE_ERR_INVALID_ARG, "batch >= 1, seq_q/seq_kv >= 0, rows < 2^31");
+  return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q,
+                  cu_seqlens_kv, batch, tq, tk, hq, hkv, d, attn_scale, mask_type, dtype, workspace,
+                  workspace_bytes, stream, nullptr, true);
 }
 
 int te_attn_read_status(const void* workspace, int* status, void* stream) {

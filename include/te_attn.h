@@ -155,6 +155,35 @@ int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* 
                        void* stream, void* dq_done);
 
 /*
+ * Sequence-major layout ("sbhd", the layout of [3216]'s reproduction: q, k, v of
+ * shape [s, b, h, d], its fp32_reference indexing q[s, b, hq, d]):
+ *   q, out, dout, dq : [seq_q,  batch, hq,  d]   16-bit, contiguous
+ *   k, v, dk, dv     : [seq_kv, batch, hkv, d]
+ *   lse              : [seq_q,  batch, hq]       fp32
+ * Token i of sequence b is row i * batch + b of the flattened [seq * batch, h, d]
+ * tensor. cu_seqlens_q/kv (int32 [batch+1]) are the prefix sums of the REAL
+ * lengths, each at most seq_q / seq_kv: tokens 0 .. len-1 of batch entry b are
+ * real and the rest are pad slots, written as exact zeros like the packed
+ * layout's (there are no padded prefix sums: every entry spans seq_* tokens).
+ * Same masks, numerics, determinism and errors as te_attn_fwd_thd /
+ * te_attn_bwd_thd; the workspace sizes are those functions' for total_q =
+ * batch * seq_q and total_kv = batch * seq_kv. Returns TE_ERR_INVALID_ARG when
+ * batch < 1, a seq_* < 0 or batch * seq_* overflows int.
+ */
+int te_attn_fwd_sbhd(const void* q, const void* k, const void* v, void* out, float* lse,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                     int seq_q, int seq_kv, int hq, int hkv, int d, float attn_scale,
+                     int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+int te_attn_bwd_sbhd(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                     int seq_q, int seq_kv, int hq, int hkv, int d, float attn_scale,
+                     int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
  * Synchronises `stream`, then copies the device status word of the last call that
  * used `workspace` into *status (0 = clean, else TE_STATUS_* bits). Returns TE_OK or
  * TE_ERR_CUDA. Intended for tests and debugging; it blocks the host.

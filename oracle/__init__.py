@@ -44,6 +44,7 @@ from .attention import (  # noqa: F401
     attn_fwd_thd,
     attn_bwd_thd,
     attn_fwd_bwd_thd,
+    attn_fwd_bwd_sbhd,
     valid_row_masks,
     fwd_bwd_flops,
 )

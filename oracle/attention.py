@@ -279,6 +279,53 @@ def attn_bwd_thd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv,
     return dq, dk, dv
 
 
+def attn_fwd_bwd_sbhd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, attn_scale, mask_type):
+    """Sequence-major forward + backward: ``q, dout [S_q, B, hq, d]``, ``k, v
+    [S_kv, B, hkv, d]`` (the layout of [3216]'s reproduction, whose
+    ``fp32_reference`` indexes ``q[s, b, hq, d]``). Batch entry b holds
+    ``cu_seqlens_*[b+1] - cu_seqlens_*[b]`` real tokens at its front; the rest are
+    pad slots. Returns ``(out, lse [S_q, B, hq], dq, dk, dv)`` float64, exactly 0 on
+    pad slots (lse 0; -inf on real queries that see no key), computed per batch
+    entry and key/value head by :func:`attn_group_fwd_bwd`.
+    Parity: pinned (equals :func:`attn_fwd_bwd_thd` on the same data laid out as
+    packed sequences)."""
+    causal = _is_causal(mask_type)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    Sq, B, hq, d = q.shape
+    Sk, Bk, hkv, _ = k.shape
+    if Bk != B:
+        raise ValueError("q and k hold different batch sizes")
+    if hkv < 1 or hq % hkv != 0:
+        raise ValueError("hq must be a positive multiple of hkv")
+    G = hq // hkv
+    lq = np.diff(np.asarray(cu_seqlens_q, dtype=np.int64))
+    lk = np.diff(np.asarray(cu_seqlens_kv, dtype=np.int64))
+    if lq.size != B or lk.size != B:
+        raise ValueError("cu_seqlens must be [B+1]")
+    if np.any(lq < 0) or np.any(lk < 0) or np.any(lq > Sq) or np.any(lk > Sk):
+        raise ValueError("real lengths must lie in [0, S]")
+    out = np.zeros((Sq, B, hq, d))
+    lse = np.zeros((Sq, B, hq))
+    dq = np.zeros((Sq, B, hq, d))
+    dk = np.zeros((Sk, B, hkv, d))
+    dv = np.zeros((Sk, B, hkv, d))
+    for b in range(B):
+        nq, nk = int(lq[b]), int(lk[b])
+        for g in range(hkv):
+            hs = slice(g * G, (g + 1) * G)
+            o, l, a, b_, c = attn_group_fwd_bwd(q[:nq, b, hs], k[:nk, b, g], v[:nk, b, g],
+                                                dout[:nq, b, hs], attn_scale, causal)
+            out[:nq, b, hs] = o
+            lse[:nq, b, hs] = l
+            dq[:nq, b, hs] = a
+            dk[:nk, b, g] = b_
+            dv[:nk, b, g] = c
+    return out, lse, dq, dk, dv
+
+
 def valid_row_masks(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                     cu_seqlens_kv_padded, T_q, T_kv, mask_type):
     """Which rows may be nonzero: ``(q_rows [T_q], kv_rows [T_kv])`` booleans.

@@ -90,7 +90,12 @@ def test_autograd_wrapper_has_no_cpu_path():
     with pytest.raises(ValueError):
         ta.DotProductAttention(2, 64, 1)(q, kv, kv, cu, cu)
     with pytest.raises(NotImplementedError):
-        ta.dot_product_attention(q, kv, kv, cu, cu, qkv_format="sbhd")
+        ta.dot_product_attention(q, kv, kv, cu, cu, qkv_format="hbsd")
+    q4, kv4 = q.view(4, 1, 2, 64), kv.view(4, 1, 1, 64)
+    with pytest.raises(ValueError):
+        ta.dot_product_attention(q4, kv4, kv4, cu, cu, qkv_format="sbhd")
+    with pytest.raises(ValueError):
+        ta.fwd_sbhd(q4, kv4, kv4, cu, cu, 0.1)
     with pytest.raises(ValueError):
         ta.DotProductAttention(3, 64, 2)
     assert {ag._mask_name(m) for m in ("causal", "padding_causal")} == {"padding_causal"}

@@ -413,6 +413,30 @@ def test_exact_zero_rows(mask):
         assert np.all(dk[o1 + 5:o1 + 7] == 0) and np.all(dv[o1 + 5:o1 + 7] == 0)
 
 
+@pytest.mark.parametrize("mask", ALL_MASKS)
+def test_sbhd_is_packed_layout_transposed(mask):
+    """The sequence-major oracle ([3216]'s layout, q[s, b, h, d]) equals the packed
+    oracle on the same values moved to rows b * S + s with padded offsets b * S,
+    for ragged real lengths below S (pad slots zero in every output)."""
+    rng = np.random.default_rng(11)
+    Sq, Sk, B, hq, hkv, d = 9, 7, 3, 4, 2, 5
+    q = rng.standard_normal((Sq, B, hq, d))
+    k = rng.standard_normal((Sk, B, hkv, d))
+    v = rng.standard_normal((Sk, B, hkv, d))
+    do = rng.standard_normal((Sq, B, hq, d))
+    lq, lk = [9, 4, 0], [5, 7, 3]
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    sb = oracle.attn_fwd_bwd_sbhd(q, k, v, do, cu_q, cu_k, 0.4, mask)
+    packed = lambda x: np.ascontiguousarray(np.swapaxes(x, 0, 1)).reshape((-1,) + x.shape[2:])
+    cp_q, cp_k = np.arange(B + 1) * Sq, np.arange(B + 1) * Sk
+    th = oracle.attn_fwd_bwd_thd(packed(q), packed(k), packed(v), packed(do), cu_q, cu_k,
+                                 cp_q, cp_k, 0.4, mask)
+    for name, a, t in zip(("out", "lse", "dq", "dk", "dv"), sb, th):
+        assert np.array_equal(packed(a), t), name
+    assert np.all(sb[0][4:, 1] == 0) and np.all(sb[0][:, 2] == 0) and np.all(sb[3][5:, 0] == 0)
+
+
 def test_golden_issue2448_zero_rows():
     """[2448] 'Expected behavior': on the second call (query lengths 0 and 3)
     the first 4 tokens of dk and dv are all zero; on the first they are not."""
