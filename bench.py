@@ -241,6 +241,27 @@ def blas_threads():
     return os.cpu_count()
 
 
+# ------------------------------------------------------------------ ranks
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """Largest value of x over all ranks: the slowest replica sets the step time.
+    (No-op for one rank; uses the default process group otherwise.)"""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_replica, ms_per_step, world):
+    """Throughput of all replicas together: each rank processes one workload per
+    step, and a step lasts as long as the slowest rank's."""
+    return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ arms
 
 
@@ -336,12 +357,8 @@ def run_ours(args, rank, world, local_rank):
     ta.profile_enable(False)
     kprof = ta.profile_read()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        x = torch.tensor([ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
-    value = world * flops / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = whole_job_tflops(flops, ms, world)
     launches = sum(c for _, c in kprof.values())
 
     # ------------------------------------------------ end to end from host buffers
@@ -434,16 +451,12 @@ def run_ours(args, rank, world, local_rank):
         e_end.record(main)
         torch.cuda.synchronize()
         barrier()
-        ems = e_start.elapsed_time(e_end) / args.steps
-        if world > 1:
-            x = torch.tensor([ems], device=dev)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            ems = float(x.item())
+        ems = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, dev)
         # the results that came back are the device results of the last step
         for got, ref in zip(host_out, (out, lse, dq, dk, dv)):
             if not torch.equal(got.view(torch.uint8), ref.cpu().view(torch.uint8)):
                 raise RuntimeError("end-to-end copies returned other bytes than the device holds")
-        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOPS",
+        e2e = {"value": whole_job_tflops(flops, ems, world), "unit": "TFLOPS",
                "ms_per_step": ems, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "overlap": "double-buffered input prefetch; outputs copied as they become final"}
 
