@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the timings of the e4m3 forward and the sequence-major layout")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["throughput", "small"], default="throughput",
                     help="small: the same recipe with 8192 real tokens (for ncu captures)")
@@ -188,7 +190,7 @@ def causal_pairs(w):
     import numpy as np
     lq = np.diff(w.cu_seqlens_q.numpy()).astype(np.float64)
     lk = np.diff(w.cu_seqlens_kv.numpy()).astype(np.float64)
-    f = 0.5 if w.mask_type == 2 else 1.0
+    f = 0.5 if w.mask_type in (2, 3) else 1.0
     return float((lq * lk * f).sum())
 
 
@@ -260,6 +262,83 @@ def whole_job_tflops(flops_per_replica, ms_per_step, world):
     """Throughput of all replicas together: each rank processes one workload per
     step, and a step lasts as long as the slowest rank's."""
     return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
+# ------------------------------------------------------------------ variants
+
+
+def time_calls(fn, flush, steps, warmup):
+    """Mean device time (ms) of fn() over `steps` calls after `warmup`, with L2
+    flushed before each call and CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        flush.fill_(1)
+        fn()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        st[i].record()
+        fn()
+        en[i].record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(st, en)) / steps
+
+
+def measure_variants(ta, w, t, flops, fwd_flops, flush, dev, steps=20, warmup=5):
+    """Device-resident timings of the library's other entry points on the same
+    sequences: the e4m3 forward (inputs quantised once with per-tensor factors
+    amax / 448) and forward + backward in the sequence-major layout (each sequence
+    the front of one [S, B, h, d] batch entry, S = the longest length)."""
+    import numpy as np
+    import torch
+    out = {}
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    cu = (t["cu_seqlens_q"], t["cu_seqlens_kv"], t["cu_seqlens_q_padded"], t["cu_seqlens_kv_padded"])
+    if f8 is not None:
+        def quant(x):
+            descale = float(x.float().abs().amax()) / 448.0
+            return (x.float() / descale).clamp(-448.0, 448.0).to(f8), descale
+        (q8, qd), (k8, kd), (v8, vd) = quant(t["q"]), quant(t["k"]), quant(t["v"])
+        o = torch.empty_like(t["q"])
+        l = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=dev)
+        Tq, hq, d = t["q"].shape
+        Tk, hkv, _ = t["k"].shape
+        ws = torch.empty(int(ta.library().te_attn_fwd_e4m3_workspace_size(w.batch, Tq, Tk, hq, hkv, d)),
+                         dtype=torch.uint8, device=dev)
+        ms = time_calls(lambda: ta.fwd_e4m3(q8, k8, v8, *cu, w.attn_scale, qd, kd, vd,
+                                            w.mask_type, out=o, lse=l, workspace=ws),
+                        flush, steps, warmup)
+        out["e4m3_forward"] = {"ms": ms, "tflops": fwd_flops / (ms * 1e-3) / 1e12,
+                               "note": "Q K^T on the e4m3 tensor path, V widened to bf16 once "
+                                       "per call, P V in bf16; includes the widening"}
+    lens = [int(x) for x in w.meta["lengths"]]
+    S, B = max(lens), len(lens)
+    offs = [int(x) for x in w.cu_seqlens_q_padded[:-1]]
+
+    def to_sbhd(x):
+        y = torch.zeros((S, B) + tuple(x.shape[1:]), dtype=x.dtype, device=dev)
+        for b in range(B):
+            y[:lens[b], b] = x[offs[b]:offs[b] + lens[b]]
+        return y
+    qs, ks, vs, dos = (to_sbhd(t[n]) for n in ("q", "k", "v", "dout"))
+    cus = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+    os_, ls = torch.empty_like(qs), torch.empty((S, B, qs.shape[2]), dtype=torch.float32, device=dev)
+    dq_, dk_, dv_ = torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)
+    wsf = torch.empty(ta.fwd_workspace_size(B, S * B, S * B, qs.shape[2], ks.shape[2], qs.shape[3]),
+                      dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ta.bwd_workspace_size(B, S * B, S * B, qs.shape[2], ks.shape[2], qs.shape[3]),
+                      dtype=torch.uint8, device=dev)
+
+    def sbhd_step():
+        ta.fwd_sbhd(qs, ks, vs, cus, cus, w.attn_scale, w.mask_type, out=os_, lse=ls, workspace=wsf)
+        ta.bwd_sbhd(qs, ks, vs, os_, dos, ls, cus, cus, w.attn_scale, w.mask_type, dq=dq_, dk=dk_,
+                    dv=dv_, workspace=wsb)
+    ms = time_calls(sbhd_step, flush, steps, warmup)
+    out["sbhd_fwd_bwd"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                           "shape": f"[{S}, {B}, h, d] with the workload's real lengths"}
+    return out
 
 
 # ------------------------------------------------------------------ arms
@@ -460,6 +539,10 @@ def run_ours(args, rank, world, local_rank):
                "ms_per_step": ems, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "overlap": "double-buffered input prefetch; outputs copied as they become final"}
 
+    variants = None
+    if not args.no_variants and args.workload == "throughput":
+        variants = measure_variants(ta, w, t, flops, 4.0 * d * pairs_h, flush, dev)
+
     if rank != 0:
         return
 
@@ -508,7 +591,7 @@ def run_ours(args, rank, world, local_rank):
                      "source": peaks["source"]},
         "flops_per_step": flops * world,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clk, "kernels": kernels, "step_ms_min": min(step_ms),
+        "clocks": clk, "kernels": kernels, "variants": variants, "step_ms_min": min(step_ms),
         "step_ms_max": max(step_ms),
     }
     print(json.dumps(line), flush=True)

@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     bwd,
     bwd_noalloc,
     fwd,
+    fwd_e4m3,
     fwd_sbhd,
     bwd_sbhd,
     fwd_workspace_size,

@@ -66,6 +66,11 @@ def library() -> ctypes.CDLL:
     L.te_attn_fwd_sbhd.argtypes = [vp] * 5 + [vp] * 2 + [i32] * 6 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_bwd_sbhd.restype = i32
     L.te_attn_bwd_sbhd.argtypes = [vp] * 9 + [vp] * 2 + [i32] * 6 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_fwd_e4m3_workspace_size.restype = sz
+    L.te_attn_fwd_e4m3_workspace_size.argtypes = [i32] * 6
+    L.te_attn_fwd_thd_e4m3.restype = i32
+    L.te_attn_fwd_thd_e4m3.argtypes = ([vp] * 5 + [vp] * 4 + [i32] * 8 + [f32] * 4 +
+                                        [i32, vp, sz, vp])
     L.te_attn_read_status.restype = i32
     L.te_attn_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     L.te_attn_last_error.restype = ctypes.c_char_p
@@ -193,6 +198,36 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
         rc = L.te_attn_bwd_thd_ev(*args, ctypes.c_void_p(dq_done.cuda_event))
     _check(rc)
     return dq, dk, dv
+
+
+def fwd_e4m3(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+             attn_scale, q_descale, k_descale, v_descale, mask_type="padding", max_seqlen_q=0,
+             max_seqlen_kv=0, out=None, lse=None, workspace=None, stream=None):
+    """``te_attn_fwd_thd_e4m3``: q, k, v ``torch.float8_e4m3fn`` (packed layout) with
+    per-tensor descale factors; returns ``(out bf16 [T_q, hq, d], lse [T_q, hq])``."""
+    L = library()
+    _need_cuda(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+               cu_seqlens_kv_padded, out, lse, workspace)
+    _cu(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded)
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None or any(t.dtype != f8 for t in (q, k, v)):
+        raise ValueError("q, k, v must be torch.float8_e4m3fn")
+    Tq, hq, d = q.shape
+    Tk, hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    out = torch.empty((Tq, hq, d), dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((Tq, hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = int(L.te_attn_fwd_e4m3_workspace_size(B, Tq, Tk, hq, hkv, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    _check(L.te_attn_fwd_thd_e4m3(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+        _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q),
+        int(max_seqlen_kv), hq, hkv, d, float(attn_scale), float(q_descale), float(k_descale),
+        float(v_descale), _mask(mask_type), _ptr(workspace), workspace.numel(),
+        ctypes.c_void_p(st)))
+    return out, lse
 
 
 def fwd_sbhd(q, k, v, cu_seqlens_q, cu_seqlens_kv, attn_scale, mask_type="padding", out=None,

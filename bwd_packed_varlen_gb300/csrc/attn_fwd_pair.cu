@@ -31,13 +31,20 @@
 
 namespace teattn {
 
-template <int kD>
+// kFP8: Q and K are e4m3 (one 128-byte column chunk per row for kD = 128) and
+// S = Q K^T runs as kind::f8f6f4; V (a bf16 copy) and O stay 16-bit.
+template <int kD, bool kFP8 = false>
 struct FwdPairShape {
   static_assert(kD == 64 || kD == 128, "two-tile forward supports head_dim up to 128");
-  static constexpr int kChunks = kD / 64;
-  static constexpr int kTileBytes = kChunks * 16384;  // 128 rows x kD cols x 2 B
-  static constexpr int kStages = 2;                   // K and V rings
-  static constexpr int kSmemUsed = kTileBytes * (2 + 2 * kStages) + 1024;
+  static_assert(!kFP8 || kD == 128, "the e4m3 forward uses 128 columns of Q and K");
+  static constexpr int kChunks = kD / 64;                      // 64-column chunks of V and O
+  static constexpr int kQKChunks = kFP8 ? kD / 128 : kChunks;  // 128-byte chunks of Q, K rows
+  static constexpr int kQKBytes = kQKChunks * 16384;           // one Q or K tile
+  static constexpr int kVBytes = kChunks * 16384;              // one V tile (16-bit)
+  static constexpr int kQKColsPerChunk = kFP8 ? 128 : 64;      // elements in 128 bytes
+  static constexpr int kSKSteps = kFP8 ? kD / 32 : kD / 16;    // MMAs per S (32 bytes of K each)
+  static constexpr int kStages = 2;                            // K and V rings
+  static constexpr int kSmemUsed = kQKBytes * (2 + kStages) + kVBytes * kStages + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
   // TMEM columns of O_x and S_x for tile x (0: A, 1: B)
   __device__ static constexpr uint32_t col_o(int x) { return static_cast<uint32_t>(x) * 128u; }
@@ -75,18 +82,19 @@ __device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool 
   return I;
 }
 
-template <int kD, bool kBF16>
+template <int kD, bool kBF16, bool kFP8 = false>
 __global__ void __launch_bounds__(kFwdPairThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
-  using S = FwdPairShape<kD>;
+  using S = FwdPairShape<kD, kFP8>;
+  static_assert(!kFP8 || kBF16, "the e4m3 forward writes bf16");
   constexpr int NS = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                          // tile A then tile B
-  uint8_t* sK = sQ + 2 * S::kTileBytes;        // NS stages
-  uint8_t* sV = sK + NS * S::kTileBytes;       // NS stages
+  uint8_t* sK = sQ + 2 * S::kQKBytes;         // NS stages
+  uint8_t* sV = sK + NS * S::kQKBytes;         // NS stages
 
   __shared__ uint64_t bar_q_full, bar_q_empty;
   __shared__ uint64_t bar_k_full[NS], bar_k_empty[NS], bar_v_full[NS], bar_v_empty[NS];
@@ -156,22 +164,22 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         nxt = next_item(p.header + kHdrNextFwd);  // used at the next hand-over
         if (ii > 0 && !(ok = mbar_wait(&bar_q_empty, (ii - 1) & 1, status))) break;
         const int ntiles = I.n[1] > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(&bar_q_full, ntiles * S::kTileBytes);
+        mbar_arrive_expect_tx(&bar_q_full, ntiles * S::kQKBytes);
         for (int x = 0; x < ntiles; ++x)
-          for (int c = 0; c < S::kChunks; ++c)
-            tma_load_4d(sQ + x * S::kTileBytes + c * 16384, &tmQ, &bar_q_full, c * 64, I.h, I.s.tb,
+          for (int c = 0; c < S::kQKChunks; ++c)
+            tma_load_4d(sQ + x * S::kQKBytes + c * 16384, &tmQ, &bar_q_full, c * S::kQKColsPerChunk, I.h, I.s.tb,
                         I.s.off_q + (2 * I.u + x) * kBlockM);
         for (int j = 0; j < I.nmax; ++j, ++it) {
           const int st = it % NS;
           if (it >= NS && !(ok = mbar_wait(&bar_k_empty[st], ((it / NS) - 1) & 1, status))) break;
-          mbar_arrive_expect_tx(&bar_k_full[st], S::kTileBytes);
-          for (int c = 0; c < S::kChunks; ++c)
-            tma_load_4d(sK + st * S::kTileBytes + c * 16384, &tmK, &bar_k_full[st], c * 64, I.g, I.s.tb,
+          mbar_arrive_expect_tx(&bar_k_full[st], S::kQKBytes);
+          for (int c = 0; c < S::kQKChunks; ++c)
+            tma_load_4d(sK + st * S::kQKBytes + c * 16384, &tmK, &bar_k_full[st], c * S::kQKColsPerChunk, I.g, I.s.tb,
                         I.s.off_k + j * kBlockN);
           if (it >= NS && !(ok = mbar_wait(&bar_v_empty[st], ((it / NS) - 1) & 1, status))) break;
-          mbar_arrive_expect_tx(&bar_v_full[st], S::kTileBytes);
+          mbar_arrive_expect_tx(&bar_v_full[st], S::kVBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_4d(sV + st * S::kTileBytes + c * 16384, &tmV, &bar_v_full[st], c * 64, I.g, I.s.tb,
+            tma_load_4d(sV + st * S::kVBytes + c * 16384, &tmV, &bar_v_full[st], c * 64, I.g, I.s.tb,
                         I.s.off_k + j * kBlockN);
         }
       }
@@ -179,7 +187,8 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
   } else if (warp == kFwdWarpMma) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBlockN);
+      constexpr uint32_t idS =
+          kFP8 ? make_idesc_e4m3(128, kBlockN) : make_idesc_f16(kBF16, false, false, 128, kBlockN);
       constexpr uint32_t idPV = make_idesc_f16(kBF16, false, true, 128, kD);
       // Q and K K-major; V as the N-major (d-contiguous) B of P V.
       const SmemDesc dq = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSW128);
@@ -191,12 +200,16 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       bool ok = true;
       // S_x = Q_x K^T for the key tile in ring stage st.
       auto issue_s = [&](int x, int st) {
-        const SmemDesc qx{dq.lo + ((x * S::kTileBytes) >> 4), dq.hi};
-        const SmemDesc kst{dk.lo + ((st * S::kTileBytes) >> 4), dk.hi};
+        const SmemDesc qx{dq.lo + ((x * S::kQKBytes) >> 4), dq.hi};
+        const SmemDesc kst{dk.lo + ((st * S::kQKBytes) >> 4), dk.hi};
 #pragma unroll
-        for (int s = 0; s < kD / 16; ++s) {
+        for (int s = 0; s < S::kSKSteps; ++s) {
+          // 32 bytes of K per MMA: 16 16-bit or 32 8-bit elements
           const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-          mma_ss(tmem + S::col_s(x), qx, off, kst, off, idS, s > 0 ? 1u : 0u);
+          if constexpr (kFP8)
+            mma_ss_f8(tmem + S::col_s(x), qx, off, kst, off, idS, s > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + S::col_s(x), qx, off, kst, off, idS, s > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s_full[x]);
       };
@@ -230,7 +243,7 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
               v_ready = true;
             }
             tc_fence_after();
-            const SmemDesc vst{dv.lo + ((st * S::kTileBytes) >> 4), dv.hi};
+            const SmemDesc vst{dv.lo + ((st * S::kVBytes) >> 4), dv.hi};
             const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int s = 0; s < kBlockN / 16; ++s)
@@ -421,16 +434,18 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
   }
 }
 
-template <int kD, bool kBF16>
+template <int kD, bool kBF16, bool kFP8 = false>
 static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
-  using S = FwdPairShape<kD>;
+  using S = FwdPairShape<kD, kFP8>;
   CUtensorMap tq, tk, tv;
   const int nb = p.sbhd ? p.batch : 1;
-  if (!make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16) ||
-      !make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16) ||
-      !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16))
+  const bool qk_ok = kFP8 ? make_tmap_tokens_u8(&tq, p.q, p.total_q, nb, p.hq, p.d) &&
+                                make_tmap_tokens_u8(&tk, p.k, p.total_kv, nb, p.hkv, p.d)
+                          : make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16) &&
+                                make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16);
+  if (!qk_ok || !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16))
     return cudaErrorInvalidValue;
-  auto kern = attn_fwd_pair_kernel<kD, kBF16>;
+  auto kern = attn_fwd_pair_kernel<kD, kBF16, kFP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -438,6 +453,11 @@ static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaSt
   const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
   kern<<<grid, kFwdPairThreads, S::kSmemBytes, st>>>(p, tq, tk, tv);
   return cudaGetLastError();
+}
+
+// e4m3 Q and K (p.q, p.k), bf16 V (p.v), bf16 out; head_dim <= 128.
+cudaError_t launch_attn_fwd_pair_e4m3(const AttnParams& p, int num_sms, cudaStream_t st) {
+  return launch_fwd_pair_impl<128, true, true>(p, num_sms, st);
 }
 
 cudaError_t launch_attn_fwd_pair(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st) {

@@ -1,8 +1,10 @@
-// Work scheduling (tile lists), exact-zero fill of rows no tile covers, and the
-// backward preprocess D = rowsum(dO * O). All three are memory- or latency-bound
-// SIMT kernels; the tensor-core kernels consume what they produce.
+// Work scheduling (tile lists), exact-zero fill of rows no tile covers, the
+// backward preprocess D = rowsum(dO * O), and the e4m3 -> bf16 widening of V for
+// the e4m3 forward. All are memory- or latency-bound SIMT kernels; the
+// tensor-core kernels consume what they produce.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cmath>
 
@@ -349,6 +351,43 @@ cudaError_t launch_delta(const AttnParams& p, bool bf16, int num_sms, cudaStream
     delta_kernel<__nv_bfloat16><<<num_sms * 8, 256, 0, st>>>(p);
   else
     delta_kernel<__half><<<num_sms * 8, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// e4m3 -> bf16 widening: dst[i] = bf16(float(src[i]) * scale), n % 16 == 0, both
+// 16-byte aligned. Each e4m3 value is exact in fp16; the product is rounded once.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ src,
+                                                         uint4* __restrict__ dst, size_t n16,
+                                                         float scale) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // two e4m3 bytes (lower one first) -> two floats
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>((w[k] >> (16 * h)) & 0xffffu), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+        o[2 * k + h] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+    }
+    dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+cudaError_t launch_widen_e4m3(const void* src, void* dst, size_t n, float scale, int num_sms,
+                              cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  widen_e4m3_kernel<<<num_sms * 8, 256, 0, st>>>(static_cast<const uint4*>(src),
+                                                  static_cast<uint4*>(dst), n / 16, scale);
   return cudaGetLastError();
 }
 

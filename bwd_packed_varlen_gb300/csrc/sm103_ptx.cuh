@@ -214,6 +214,14 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, bool a_mn, bool
          ((static_cast<uint32_t>(M) >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor for kind::f8f6f4 with A and B both e4m3 (format code 0),
+// both K-major, D fp32.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+  return (1u << 4) |                               // D format: f32
+         ((static_cast<uint32_t>(N) >> 3) << 17) | // N / 8
+         ((static_cast<uint32_t>(M) >> 4) << 24);  // M / 16
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: MMA issue (single thread) and completion
 // ---------------------------------------------------------------------------
@@ -244,6 +252,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SmemDes
       "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %5, 0;\n mov.b64 db, {%2, %3};\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// kind::f8f6f4 (8-bit A and B from shared memory, K = 32 per instruction), with
+// split descriptors plus byte offsets added to their start addresses.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, SmemDesc a, uint32_t a_off, SmemDesc b,
+                                          uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n"
+      " mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc),
+      "r"(accumulate)
       : "memory");
 }
 

@@ -215,13 +215,26 @@ size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
   return make_layout(batch, total_q, total_kv, hq, true, &L) ? L.total : 0;
 }
 
+// Per-tensor dequantisation factors of an e4m3 forward (real value = stored
+// value * descale); `on` false for 16-bit inputs.
+struct E4m3Scales {
+  bool on;
+  float q, k, v;
+};
+
+// Bytes of the widened (bf16) V copy an e4m3 forward keeps after the layout.
+size_t widened_v_bytes(int total_kv, int hkv, int d) {
+  return align_up(static_cast<size_t>(total_kv > 0 ? total_kv : 0) * hkv * d * 2, 256);
+}
+
 // Forward of either layout: sbhd = false packs sequences by cu_seqlens_*_padded,
 // sbhd = true puts token i of sequence b at row i * batch + b.
 static int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
                     const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int batch,
                     int total_q, int total_kv, int hq, int hkv, int d, float attn_scale, int mask_type,
-                    int dtype, void* workspace, size_t workspace_bytes, void* stream, bool sbhd) {
+                    int dtype, void* workspace, size_t workspace_bytes, void* stream, bool sbhd,
+                    E4m3Scales e4m3 = E4m3Scales{false, 1.f, 1.f, 1.f}) {
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
                         cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                         workspace);
@@ -231,35 +244,52 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   if (total_kv > 0 && (!k || !v)) return fail(TE_ERR_INVALID_ARG, "k and v must not be NULL");
   if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (out && !aligned16(out)))
     return fail(TE_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+  if (e4m3.on) {
+    if (d % 16 != 0 || d > 128)
+      return fail(TE_ERR_UNSUPPORTED, "the e4m3 forward needs head dim a multiple of 16, <= 128");
+    if (!(e4m3.q > 0.f) || !(e4m3.k > 0.f) || !(e4m3.v > 0.f) || !std::isfinite(e4m3.q) ||
+        !std::isfinite(e4m3.k) || !std::isfinite(e4m3.v))
+      return fail(TE_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+  }
   Layout L;
   if (!make_layout(batch, total_q, total_kv, hq, false, &L))
     return fail(TE_ERR_INVALID_ARG, "sizes out of range");
-  if (workspace_bytes < L.total)
-    return fail(TE_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than te_attn_fwd_workspace_size()");
+  const size_t need = L.total + (e4m3.on ? widened_v_bytes(total_kv, hkv, d) : 0);
+  if (workspace_bytes < need)
+    return fail(TE_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than the *_workspace_size() answer");
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return fail(TE_ERR_CUDA, "no CUDA device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // e4m3: the softmax sees attn_scale * q_descale * k_descale times the e4m3 dot product
+  const float scale = e4m3.on ? attn_scale * e4m3.q * e4m3.k : attn_scale;
   teattn::AttnParams p = base_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                                      cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d,
-                                     attn_scale, mask_type, workspace, L);
+                                     scale, mask_type, workspace, L);
   if (sbhd) {
     p.sbhd = 1;
     p.rs = batch;
   }
+  char* ws = static_cast<char*>(workspace);
   p.q = q;
   p.k = k;
-  p.v = v;
+  p.v = e4m3.on ? static_cast<const void*>(ws + L.total) : v;
   p.out = out;
   p.lse = lse;
   p.sched_lists = d <= 128 ? teattn::kListF : teattn::kListQ;
-  char* ws = static_cast<char*>(workspace);
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
   const bool bf16 = dtype == TE_DTYPE_BF16;
   cudaError_t e = timed(TE_KERNEL_SCHEDULE, st, [&] { return teattn::launch_schedule(p, pref_q, pref_k, reinterpret_cast<int*>(ws + L.pref_f), st); });
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  if (e4m3.on && total_kv > 0) {
+    // every row of V, pad slots included (they are finite e4m3 values)
+    e = teattn::launch_widen_e4m3(v, ws + L.total, static_cast<size_t>(total_kv) * hkv * d, e4m3.v,
+                                  sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "widen V");
+  }
   if (total_q > 0 && total_kv > 0) {
     e = timed(TE_KERNEL_FWD, st, [&] {
+      if (e4m3.on) return teattn::launch_attn_fwd_pair_e4m3(p, sms, st);
       return d <= 128 ? teattn::launch_attn_fwd_pair(p, bf16, sms, st)
                       : teattn::launch_attn_fwd(p, bf16, sms, st);
     });
@@ -302,6 +332,28 @@ int te_attn_fwd_sbhd(const void* q, const void* k, const void* v, void* out, flo
   return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q, cu_seqlens_kv,
                   batch, tq, tk, hq, hkv, d, attn_scale, mask_type, dtype, workspace,
                   workspace_bytes, stream, true);
+}
+
+size_t te_attn_fwd_e4m3_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                       int d) {
+  Layout L;
+  if (!make_layout(batch, total_q, total_kv, hq, false, &L)) return 0;
+  return L.total + widened_v_bytes(total_kv, hkv, d);
+}
+
+int te_attn_fwd_thd_e4m3(const void* q, const void* k, const void* v, void* out, float* lse,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                         const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                         int batch, int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                         int hq, int hkv, int d, float attn_scale, float q_descale, float k_descale,
+                         float v_descale, int mask_type, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
+  return fwd_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
+                  TE_DTYPE_BF16, workspace, workspace_bytes, stream, false,
+                  E4m3Scales{true, q_descale, k_descale, v_descale});
 }
 
 static int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,

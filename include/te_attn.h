@@ -184,6 +184,32 @@ int te_attn_bwd_sbhd(const void* q, const void* k, const void* v, const void* ou
                      void* stream);
 
 /*
+ * e4m3 forward (no counterpart in the pages' code; [2892] is the report of TE's
+ * FP8 forward failing when cu_seqlens_q != cu_seqlens_q_padded -- out of bounds
+ * and an unpadded output -- and this entry keeps that case exact): q, k, v hold
+ * FP8 e4m3 bytes in the packed layout ([total_q, hq, d], [total_kv, hkv, d]) with
+ * per-tensor dequantisation factors (real value = stored value * descale), out is
+ * bf16 [total_q, hq, d] and lse fp32 [total_q, hq], both in the padded layout with
+ * the same exact-zero rows as te_attn_fwd_thd. Scores are formed on the e4m3
+ * tensor-core path (attn_scale * q_descale * k_descale times the e4m3 dot
+ * products, fp32 accumulation); V is widened once to bf16 (times v_descale) in
+ * the workspace and P V runs in bf16 like te_attn_fwd_thd. Needs d a multiple of
+ * 16 with d <= 128, descale factors finite and > 0, and a workspace of
+ * te_attn_fwd_e4m3_workspace_size() bytes. Same masks, determinism and errors as
+ * te_attn_fwd_thd otherwise.
+ */
+size_t te_attn_fwd_e4m3_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                       int d);
+
+int te_attn_fwd_thd_e4m3(const void* q, const void* k, const void* v, void* out, float* lse,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                         const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                         int batch, int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                         int hq, int hkv, int d, float attn_scale, float q_descale, float k_descale,
+                         float v_descale, int mask_type, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
  * Synchronises `stream`, then copies the device status word of the last call that
  * used `workspace` into *status (0 = clean, else TE_STATUS_* bits). Returns TE_OK or
  * TE_ERR_CUDA. Intended for tests and debugging; it blocks the host.

@@ -45,6 +45,7 @@ from .attention import (  # noqa: F401
     attn_bwd_thd,
     attn_fwd_bwd_thd,
     attn_fwd_bwd_sbhd,
+    attn_fwd_thd_e4m3,
     valid_row_masks,
     fwd_bwd_flops,
 )

@@ -279,6 +279,24 @@ def attn_bwd_thd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv,
     return dq, dk, dv
 
 
+def attn_fwd_thd_e4m3(q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens_q,
+                      cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, attn_scale,
+                      mask_type):
+    """Forward from 8-bit e4m3 inputs with per-tensor dequantisation factors:
+    ``q8, k8, v8`` are the e4m3 values already decoded to numbers (the stored byte's
+    value), and the attention runs on ``q8 * q_descale`` etc. exactly as
+    :func:`attn_fwd_thd` does. The pages give no FP8 arithmetic beyond [2892]'s
+    failing forward with real != padded lengths; the per-tensor factors are this
+    package's reading. Returns ``(out, lse)`` float64.
+    Parity: pinned through :func:`attn_fwd_thd` (the e4m3 decoding it relies on is
+    pinned against the format's definition in the tests)."""
+    q = np.asarray(q8, dtype=np.float64) * float(q_descale)
+    k = np.asarray(k8, dtype=np.float64) * float(k_descale)
+    v = np.asarray(v8, dtype=np.float64) * float(v_descale)
+    return attn_fwd_thd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                        cu_seqlens_kv_padded, attn_scale, mask_type)
+
+
 def attn_fwd_bwd_sbhd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, attn_scale, mask_type):
     """Sequence-major forward + backward: ``q, dout [S_q, B, hq, d]``, ``k, v
     [S_kv, B, hkv, d]`` (the layout of [3216]'s reproduction, whose

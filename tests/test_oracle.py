@@ -437,6 +437,39 @@ def test_sbhd_is_packed_layout_transposed(mask):
     assert np.all(sb[0][4:, 1] == 0) and np.all(sb[0][:, 2] == 0) and np.all(sb[3][5:, 0] == 0)
 
 
+def test_e4m3_decoding_matches_the_format():
+    """The e4m3 values the GPU tests hand to the oracle come from torch's
+    float8_e4m3fn decoding; every one of the 254 finite codes equals the format's
+    definition: sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals at
+    exponent 0, and 0x7f / 0xff are NaN (no infinities)."""
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    got = codes.view(f8).to(torch.float64).numpy()
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            assert np.isnan(got[c])
+            continue
+        mag = 2.0 ** (e - 7) * (1 + m / 8) if e > 0 else 2.0 ** -6 * (m / 8)
+        assert got[c] == (-mag if s else mag), c
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_e4m3_forward_is_the_dequantised_forward():
+    """The e4m3 forward of the oracle equals the float64 forward on the
+    dequantised inputs (values times their per-tensor factors)."""
+    q, k, v, do, cu_q, cu_k, cp_q, cp_k = _rand_case(31, [5, 9], [7, 4], [6, 9], [8, 4], 4, 2, 16)
+    r8 = lambda x: np.round(x * 8) / 8  # any representable values will do here
+    a = oracle.attn_fwd_thd_e4m3(r8(q), r8(k), r8(v), 0.5, 0.25, 2.0, cu_q, cu_k, cp_q, cp_k,
+                                 0.3, MASK_PADDING_CAUSAL)
+    b = oracle.attn_fwd_thd(r8(q) * 0.5, r8(k) * 0.25, r8(v) * 2.0, cu_q, cu_k, cp_q, cp_k, 0.3,
+                            MASK_PADDING_CAUSAL)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
 def test_golden_issue2448_zero_rows():
     """[2448] 'Expected behavior': on the second call (query lengths 0 and 3)
     the first 4 tokens of dk and dv are all zero; on the first they are not."""
