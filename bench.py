@@ -591,7 +591,8 @@ def run_ours(args, rank, world, local_rank):
                      "source": peaks["source"]},
         "flops_per_step": flops * world,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clk, "kernels": kernels, "variants": variants, "step_ms_min": min(step_ms),
+        "clocks": clk, "kernels": kernels, "variants": variants,
+        "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
         "step_ms_max": max(step_ms),
     }
     print(json.dumps(line), flush=True)

@@ -102,3 +102,48 @@ def test_autograd_wrapper_has_no_cpu_path():
     assert ag._mask_name("causal_bottom_right") == "padding_causal_bottom_right"
     assert ag._mask_name("no_mask") == "padding"
     assert ta._binding._mask("padding_causal_bottom_right") == 3
+
+
+def test_host_checked_errors_launch_nothing(lib):
+    """Argument errors the host can see return their code before any device work,
+    so they are checked here without a GPU (the pointers are placeholders that the
+    library never dereferences on these paths)."""
+    import ctypes
+    P = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never touched
+    cu = ctypes.c_void_p(1 << 21)
+    big = ctypes.c_size_t(1 << 40)
+
+    def fwd(**kw):
+        a = dict(batch=2, tq=64, tk=64, hq=4, hkv=2, d=64, scale=0.1, mask=1, dtype=1, ws=P, wsb=big)
+        a.update(kw)
+        return lib.te_attn_fwd_thd(P, P, P, P, P, cu, cu, cu, cu, a["batch"], a["tq"], a["tk"], 0, 0,
+                                   a["hq"], a["hkv"], a["d"], a["scale"], a["mask"], a["dtype"],
+                                   a["ws"], a["wsb"], None)
+    assert fwd(mask=4) == -2                      # unknown mask type
+    assert fwd(hq=3) == -1                        # hq not a multiple of hkv
+    assert fwd(d=12) == -2                        # head dim not a multiple of 8
+    assert fwd(d=264) == -2                       # head dim above 256
+    assert fwd(batch=0) == -1
+    assert fwd(dtype=7) == -2
+    assert fwd(scale=float("inf")) == -1
+    assert fwd(ws=None) == -1
+    assert fwd(wsb=ctypes.c_size_t(16)) == -3     # workspace too small
+    assert lib.te_attn_last_error()
+
+    def e4m3(d=64, descale=1.0, wsb=big):
+        return lib.te_attn_fwd_thd_e4m3(P, P, P, P, P, cu, cu, cu, cu, 2, 64, 64, 0, 0, 4, 2, d,
+                                        0.1, descale, 1.0, 1.0, 1, P, wsb, None)
+    assert e4m3(d=40) == -2                       # e4m3 needs d % 16 == 0
+    assert e4m3(d=144) == -2                      # and d <= 128
+    assert e4m3(descale=0.0) == -1
+    assert e4m3(descale=float("nan")) == -1
+    assert e4m3(wsb=ctypes.c_size_t(lib.te_attn_fwd_workspace_size(2, 64, 64, 4, 2, 64))) == -3
+    assert (lib.te_attn_fwd_e4m3_workspace_size(2, 64, 64, 4, 2, 64)
+            == lib.te_attn_fwd_workspace_size(2, 64, 64, 4, 2, 64) + 64 * 2 * 64 * 2)
+
+    assert lib.te_attn_fwd_sbhd(P, P, P, P, P, cu, cu, 0, 8, 8, 4, 2, 64, 0.1, 1, 1, P, big,
+                                None) == -1       # batch < 1
+    assert lib.te_attn_bwd_sbhd(P, P, P, P, P, P, P, P, P, cu, cu, 2, -1, 8, 4, 2, 64, 0.1, 1, 1,
+                                P, big, None) == -1  # negative length
+    assert lib.te_attn_fwd_sbhd(P, P, P, P, P, cu, cu, 2, 1 << 30, 8, 4, 2, 64, 0.1, 1, 1, P, big,
+                                None) == -1       # rows overflow int
