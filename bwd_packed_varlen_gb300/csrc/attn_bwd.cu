@@ -649,15 +649,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
           if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
+          // Early-S order: dP_j+1 goes ahead of dQ_j (its region was read before
+          // ds_ready_j), so the compute warps start on dS_j+1 while the tensor
+          // cores run dQ_j; a commit after dQ_j hands K stage j back.
+          if (kEarlyS && more) issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
           const SmemDesc kst{dk_mn.lo + ((cur % KS) * S::kKVBytes >> 4), dk_mn.hi};
           const uint32_t a_ds = t_ds + (cur & 1) * S::kDsCols;
           const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2)
             mma_ts(t_dq, a_ds + s2 * 8, kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);
+          if (kEarlyS) mma_commit(&bar_k_empty[cur % KS]);
           if (!kEarlyS && more) issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
-          // dp_full of step j+1 also covers dQ_j: K_j is free once it fires
-          if (more) issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
+          // here dp_full of step j+1 also covers dQ_j: K_j is free once it fires
+          if (!kEarlyS && more) issue_s((cur + 1) % VS, t_dp, ddo, dv, &bar_dp_full);
           if (j + 2 == n) mma_commit(&bar_q_empty);
         }
         if (!ok) break;
@@ -736,10 +741,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if (tid == 0) {
-          // dP_it is done, so V stage it is free; past an item's first step the
-          // commit also covered dQ_(it-1), which was the last reader of K stage it-1.
+          // dP_it is done, so V stage it is free; without early S, past an item's
+          // first step the commit also covered dQ_(it-1), the last reader of K
+          // stage it-1 (with early S the MMA thread commits K stages itself).
           mbar_arrive(&bar_v_empty[it % VS]);
-          if (j > 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);
+          if (!kEarlyS && j > 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);
         }
         {
           uint32_t dv[kG];
@@ -771,7 +777,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
-      if (tid == 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);  // dQ of the item's last step
+      if (!kEarlyS && tid == 0) mbar_arrive(&bar_k_empty[(it - 1) % KS]);  // the item's last dQ
       const auto rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dq) + cur.gi * p.d, cur.row_valid);
       constexpr int kOutCols = kD / kColGroups;
 #pragma unroll
