@@ -636,8 +636,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (n == 1) mma_commit(&bar_q_empty);
         // Two hand-overs per step. The compute warps arrive on s_free once they
         // have read S_j and K_j+1 has landed, and on ds_ready once dS_j is written
-        // (dP_j read) and V_j+1 has landed; they also hand the K/V stages back to
-        // the producer, so this thread never stops for ring bookkeeping.
+        // (dP_j read) and V_j+1 has landed; they hand the V stages (and, without
+        // early S, the K stages) back to the producer. With early S this thread
+        // returns K stage j by a commit behind dQ_j, its last reader.
         for (int j = 0; j < n; ++j) {
           const int cur = it + j;
           const bool more = j + 1 < n;
