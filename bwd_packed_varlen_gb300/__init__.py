@@ -4,6 +4,13 @@ The compute lives in ``lib/libteattn.so`` (C ABI in ``include/te_attn.h``); this
 package marshals torch tensors into that ABI and nothing more. There is no CPU
 path: every function raises if the library is missing or a tensor is not on a
 CUDA device.
+
+Entry points: ``fwd`` / ``bwd`` (packed THD layout, real and padded cu_seqlens),
+``fwd_sbhd`` / ``bwd_sbhd`` (sequence-major ``[S, B, h, d]``), ``fwd_e4m3`` (e4m3
+inputs with per-tensor descale factors, forward only), ``bwd_noalloc`` (backward
+without a workspace); masks ``padding``, ``padding_causal`` (upper-left) and
+``padding_causal_bottom_right``. ``dot_product_attention`` / ``DotProductAttention``
+wrap them for autograd (``thd``, ``bshd``, ``sbhd``).
 """
 
 from ._binding import (  # noqa: F401
