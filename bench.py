@@ -540,7 +540,7 @@ def run_ours(args, rank, world, local_rank):
                "overlap": "double-buffered input prefetch; outputs copied as they become final"}
 
     variants = None
-    if not args.no_variants and args.workload == "throughput":
+    if not args.no_variants:
         variants = measure_variants(ta, w, t, flops, 4.0 * d * pairs_h, flush, dev)
 
     if rank != 0:
