@@ -8,7 +8,9 @@ CUDA device.
 Entry points: ``fwd`` / ``bwd`` (packed THD layout, real and padded cu_seqlens),
 ``fwd_sbhd`` / ``bwd_sbhd`` (sequence-major ``[S, B, h, d]``), ``fwd_e4m3`` (e4m3
 inputs with per-tensor descale factors, forward only), ``bwd_noalloc`` (backward
-without a workspace); masks ``padding``, ``padding_causal`` (upper-left) and
+without a workspace); ``read_status`` / ``read_status_noalloc`` read a call's device
+status word, ``selftest_wait_timeout`` runs the bounded-wait unwind path on purpose and
+``debug_build()`` routes calls to the bounds-checking build; masks ``padding``, ``padding_causal`` (upper-left) and
 ``padding_causal_bottom_right``. ``dot_product_attention`` / ``DotProductAttention``
 wrap them for autograd (``thd``, ``bshd``, ``sbhd``).
 """
@@ -20,6 +22,7 @@ from ._binding import (  # noqa: F401
     TeAttnError,
     bwd,
     bwd_noalloc,
+    debug_build,
     fwd,
     fwd_e4m3,
     fwd_sbhd,
@@ -32,6 +35,8 @@ from ._binding import (  # noqa: F401
     library,
     library_path,
     read_status,
+    read_status_noalloc,
+    selftest_wait_timeout,
     version,
 )
 from .autograd import (  # noqa: F401

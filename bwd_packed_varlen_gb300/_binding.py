@@ -8,6 +8,7 @@ torch when the caller does not supply them.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -22,7 +23,9 @@ _DTYPES = {torch.float16: 0, torch.bfloat16: 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libteattn.so")
-_lib = None
+_LIB_DEBUG_PATH = os.path.join(_HERE, "lib", "libteattn_debug.so")
+_libs = {}
+_use_debug = False
 
 
 class TeAttnError(RuntimeError):
@@ -33,20 +36,36 @@ class TeAttnError(RuntimeError):
         self.code = code
 
 
-def library_path() -> str:
-    return _LIB_PATH
+def library_path(debug: bool = False) -> str:
+    return _LIB_DEBUG_PATH if debug else _LIB_PATH
 
 
-def library() -> ctypes.CDLL:
-    """Load libteattn.so (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(_LIB_PATH):
+@contextlib.contextmanager
+def debug_build():
+    """Within this block every call goes to ``libteattn_debug.so``, the build that
+    bounds-checks each computed global offset and records a bad one as
+    ``TE_STATUS_OUT_OF_BOUNDS`` (bit 4) in the call's status word."""
+    global _use_debug
+    old = _use_debug
+    _use_debug = True
+    try:
+        yield library(debug=True)
+    finally:
+        _use_debug = old
+
+
+def library(debug: bool = None) -> ctypes.CDLL:
+    """Load libteattn.so, or its debug build (raises if it has not been built).
+    ``debug=None`` picks the build selected by :func:`debug_build`."""
+    debug = _use_debug if debug is None else bool(debug)
+    if debug in _libs:
+        return _libs[debug]
+    path = library_path(debug)
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+            f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; "
             "g.build()'` (or python bwd_packed_varlen_gb300/build.py)")
-    L = ctypes.CDLL(_LIB_PATH)
+    L = ctypes.CDLL(path)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.te_attn_version.restype = i32
     L.te_attn_version.argtypes = []
@@ -79,7 +98,11 @@ def library() -> ctypes.CDLL:
     L.te_attn_profile_enable.argtypes = [i32]
     L.te_attn_profile_read.restype = i32
     L.te_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
-    _lib = L
+    L.te_attn_read_status_noalloc.restype = i32
+    L.te_attn_read_status_noalloc.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+    L.te_attn_selftest_wait_timeout.restype = i32
+    L.te_attn_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint, vp]
+    _libs[debug] = L
     return L
 
 
@@ -102,6 +125,12 @@ def _check(rc: int):
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _on(t):
+    """Make t's device current for the call: the library launches on, and looks up
+    per-device state of, the current device."""
+    return torch.cuda.device(t.device)
 
 
 def _need_cuda(*ts):
@@ -150,11 +179,12 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    rc = L.te_attn_fwd_thd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
-        _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk,
-        int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, d, float(attn_scale), _mask(mask_type),
-        _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st))
+    with _on(q):
+        rc = L.te_attn_fwd_thd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+            _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk,
+            int(max_seqlen_q), int(max_seqlen_kv), hq, hkv, d, float(attn_scale), _mask(mask_type),
+            _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st))
     _check(rc)
     return out, lse
 
@@ -189,13 +219,14 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
             _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
             d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace),
             workspace.numel(), ctypes.c_void_p(st))
-    if dq_done is None:
-        rc = L.te_attn_bwd_thd(*args)
-    else:
-        if dq_done.cuda_event == 0:  # torch creates the CUDA event on its first record
-            dq_done.record(torch.cuda.ExternalStream(st) if stream is not None
-                           else torch.cuda.current_stream(q.device))
-        rc = L.te_attn_bwd_thd_ev(*args, ctypes.c_void_p(dq_done.cuda_event))
+    with _on(q):
+        if dq_done is None:
+            rc = L.te_attn_bwd_thd(*args)
+        else:
+            if dq_done.cuda_event == 0:  # torch creates the CUDA event on its first record
+                dq_done.record(torch.cuda.ExternalStream(st) if stream is not None
+                               else torch.cuda.current_stream(q.device))
+            rc = L.te_attn_bwd_thd_ev(*args, ctypes.c_void_p(dq_done.cuda_event))
     _check(rc)
     return dq, dk, dv
 
@@ -221,12 +252,13 @@ def fwd_e4m3(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqle
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    _check(L.te_attn_fwd_thd_e4m3(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
-        _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q),
-        int(max_seqlen_kv), hq, hkv, d, float(attn_scale), float(q_descale), float(k_descale),
-        float(v_descale), _mask(mask_type), _ptr(workspace), workspace.numel(),
-        ctypes.c_void_p(st)))
+    with _on(q):
+        _check(L.te_attn_fwd_thd_e4m3(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+            _ptr(cu_seqlens_q_padded), _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q),
+            int(max_seqlen_kv), hq, hkv, d, float(attn_scale), float(q_descale), float(k_descale),
+            float(v_descale), _mask(mask_type), _ptr(workspace), workspace.numel(),
+            ctypes.c_void_p(st)))
     return out, lse
 
 
@@ -249,10 +281,11 @@ def fwd_sbhd(q, k, v, cu_seqlens_q, cu_seqlens_kv, attn_scale, mask_type="paddin
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    _check(L.te_attn_fwd_sbhd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
-        B, Sq, Sk, hq, hkv, d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype],
-        _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
+    with _on(q):
+        _check(L.te_attn_fwd_sbhd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+            B, Sq, Sk, hq, hkv, d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype],
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
     return out, lse
 
 
@@ -277,10 +310,11 @@ def bwd_sbhd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, attn_scale,
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    _check(L.te_attn_bwd_sbhd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-        _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Sq, Sk, hq, hkv, d, float(attn_scale),
-        _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
+    with _on(q):
+        _check(L.te_attn_bwd_sbhd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, Sq, Sk, hq, hkv, d, float(attn_scale),
+            _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace), workspace.numel(), ctypes.c_void_p(st)))
     return dq, dk, dv
 
 
@@ -290,11 +324,12 @@ def read_status(workspace, stream=None) -> int:
     L = library()
     st = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
     val = ctypes.c_int(0)
-    _check(L.te_attn_read_status(_ptr(workspace), ctypes.byref(val), ctypes.c_void_p(st)))
+    with _on(workspace):
+        _check(L.te_attn_read_status(_ptr(workspace), ctypes.byref(val), ctypes.c_void_p(st)))
     return int(val.value)
 
 
-KERNELS = ("schedule", "fwd", "zero_fill", "delta", "dkdv", "dq")
+KERNELS = ("schedule", "fwd", "zero_fill", "delta", "dkdv", "dq", "widen_e4m3")
 
 
 def profile_enable(on: bool = True) -> None:
@@ -330,10 +365,35 @@ def bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
-    rc = L.te_attn_bwd_thd_noalloc(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
-        _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
-        _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
-        d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], ctypes.c_void_p(st))
+    with _on(q):
+        rc = L.te_attn_bwd_thd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(cu_seqlens_q_padded),
+            _ptr(cu_seqlens_kv_padded), B, Tq, Tk, int(max_seqlen_q), int(max_seqlen_kv), hq, hkv,
+            d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], ctypes.c_void_p(st))
     _check(rc)
     return dq, dk, dv
+
+
+def read_status_noalloc(device=None, stream=None) -> int:
+    """``te_attn_read_status_noalloc``: synchronise and return the status word of the
+    last :func:`bwd_noalloc` call on ``device`` (default: the current device)."""
+    L = library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+        val = ctypes.c_int(0)
+        _check(L.te_attn_read_status_noalloc(ctypes.byref(val), ctypes.c_void_p(st)))
+    return int(val.value)
+
+
+def selftest_wait_timeout(workspace, limit_us: int = 1000, stream=None) -> None:
+    """``te_attn_selftest_wait_timeout``: launch the bounded-wait unwind self-test on
+    ``workspace`` (a CUDA uint8 tensor of at least 256 bytes); read the outcome with
+    :func:`read_status` and the workspace's header words 8..11."""
+    L = library()
+    _need_cuda(workspace)
+    with _on(workspace):
+        st = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
+        _check(L.te_attn_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_us),
+                                               ctypes.c_void_p(st)))

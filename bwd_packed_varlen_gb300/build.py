@@ -1,7 +1,10 @@
 """Build libteattn.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
 Each .cu file compiles in its own nvcc process, in parallel, then one link step
-produces ``bwd_packed_varlen_gb300/lib/libteattn.so``. Objects go to ``_build/``.
+per library produces ``bwd_packed_varlen_gb300/lib/libteattn.so`` and its debug
+build ``libteattn_debug.so`` (compiled with ``TEATTN_DEBUG_BOUNDS``: every computed
+global offset is checked and a bad one is recorded as ``TE_STATUS_OUT_OF_BOUNDS``
+in the call's status word instead of being accessed). Objects go to ``_build/``.
 """
 
 from __future__ import annotations
@@ -17,10 +20,12 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "lib", "libteattn.so")
+LIB_DEBUG = os.path.join(PKG, "lib", "libteattn_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
+VARIANTS = {"release": (LIB, []), "debug": (LIB_DEBUG, ["-DTEATTN_DEBUG_BOUNDS"])}
 
 
 def nvcc() -> str:
@@ -34,9 +39,10 @@ def _sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(job) -> str:
+    src, variant, verbose = job
+    obj = os.path.join(BUILD, variant, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *VARIANTS[variant][1], "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -47,19 +53,26 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Compile every kernel source and link the shared library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, variants=("release", "debug")) -> str:
+    """Compile every kernel source for each variant and link the shared libraries;
+    returns the path of the release library."""
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
     srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = []
+    for v in variants:
+        os.makedirs(os.path.join(BUILD, v), exist_ok=True)
+        jobs += [(s, v, verbose and v == "release") for s in srcs]
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(_compile, jobs))
+    for v in variants:
+        lib = VARIANTS[v][0]
+        vobjs = [o for o, j in zip(objs, jobs) if j[1] == v]
+        tmp = lib + ".tmp"
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *vobjs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

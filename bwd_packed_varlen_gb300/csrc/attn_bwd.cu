@@ -215,7 +215,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_4d(sDO + st * S::kQBytes + c * kBM * 128, &tmDO, &bar_q_full[st], c * 64, h, I.s.tb,
                         I.s.off_q + qt * kBM);
           }
-          const size_t ti = tiled_index(p, I.b, qt * kBM, h);
+          size_t ti = tiled_index(p, I.b, qt * kBM, h);
+          // a bad offset still completes the barrier's byte count, from row 0
+          if (!bounds_ok(ti + kBM <= static_cast<size_t>(p.pair_cap_q) * p.hq * kBlockM, status)) ti = 0;
           bulk_load(sLse + st * kBM, p.lse_t + ti, kBM * 4, &bar_q_full[st]);
           bulk_load(sDelta + st * kBM, p.delta_t + ti, kBM * 4, &bar_q_full[st]);
         }
@@ -417,9 +419,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full, ii & 1, status));
       if (!ok) break;
       tc_fence_after();
-      const bool store = kv_row < seen_keys(I.s, causal);
-      const size_t kv_off =
-          ((static_cast<size_t>(kv_row0) + static_cast<size_t>(kv_row) * p.rs) * p.hkv + I.g) * p.d;
+      const size_t kv_tok = static_cast<size_t>(kv_row0) + static_cast<size_t>(kv_row) * p.rs;
+      const bool store = kv_row < seen_keys(I.s, causal) &&
+                         bounds_ok(kv_tok < static_cast<size_t>(p.total_kv), status);
+      const size_t kv_off = (kv_tok * p.hkv + I.g) * p.d;
       const auto dk_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dk) + kv_off, store);
       const auto dv_rows = make_row_pair(static_cast<elem_t<kBF16>*>(p.dv) + kv_off, store);
       const int col_out = I.split * S::kDo;
@@ -695,9 +698,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int row = pr.y * kBlockM + quarter * 32 + lane;
       // rows that see no key (before a lower-right triangle) are the zero fill's
       r.lim = row < s.len_q ? row_keys(s, row, causal) : 0;
-      r.row_valid = r.lim > 0;
       r.gi = q_row(p, s, row) * p.hq + h;
       const size_t ti = tiled_index(p, pr.x, row, h);
+      r.row_valid = r.lim > 0 &&
+                    bounds_ok(r.gi < static_cast<size_t>(p.total_q) * p.hq &&
+                                  ti < static_cast<size_t>(p.pair_cap_q) * p.hq * kBlockM,
+                              status);
       r.lse2 = r.row_valid ? p.lse_t[ti] : 0.f;
       r.dlt = r.row_valid ? p.delta_t[ti] : 0.f;
       return r;

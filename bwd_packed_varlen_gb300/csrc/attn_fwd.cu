@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(192, 1)
       const int row = qt * kBlockM + tid;
       // rows that see no key (before a lower-right triangle) are the zero fill's
       const int lim = row < s.len_q ? row_keys(s, row, causal) : 0;
-      const bool row_valid = lim > 0;
+      const bool row_valid = lim > 0 && bounds_ok(q_row(p, s, row) < static_cast<size_t>(p.total_q),
+                                                  p.header + kHdrStatus);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const int cur = it + j;

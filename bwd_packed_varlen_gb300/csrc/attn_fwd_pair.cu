@@ -299,8 +299,9 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       const int row = (2 * I.u + x) * kBlockM + quarter * 32 + lane;
       // rows that see no key (before a lower-right triangle) are the zero fill's
       r.lim = row < I.s.len_q ? row_keys(I.s, row, causal) : 0;
-      r.row_valid = r.lim > 0;
       r.out_row = q_row(p, I.s, row) * p.hq + I.h;
+      r.row_valid = r.lim > 0 &&
+                    bounds_ok(r.out_row < static_cast<size_t>(p.total_q) * p.hq, p.header + kHdrStatus);
       return r;
     };
     RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));

@@ -23,6 +23,7 @@ enum HeaderWord : int {
   kHdrNextDkdv = 4,
   kHdrNextDq = 5,
   kHdrNumFPairs = 6, // number of (sequence, 256-row query tile pair) items
+  kHdrSelftest = 8,  // words 8..11: results of te_attn_selftest_wait_timeout
   kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
 };
 
@@ -31,6 +32,23 @@ constexpr int kListQ = 1, kListK = 2, kListF = 4;
 
 constexpr int kStatusBadSeqlens = 1;
 constexpr int kStatusTimeout = 2;
+constexpr int kStatusOutOfBounds = 4;
+
+// Bounds checks of computed global offsets. In the debug build of the library
+// (TEATTN_DEBUG_BOUNDS defined) a failed check records kStatusOutOfBounds in the
+// call's status word and the caller skips the access; in the release build the
+// check compiles to `true` and costs nothing. Never a trap or an assert: the
+// status word is read by the host after the call.
+__device__ __forceinline__ bool bounds_ok(bool in_bounds, int* status) {
+#ifdef TEATTN_DEBUG_BOUNDS
+  if (!in_bounds) atomicOr(status, kStatusOutOfBounds);
+  return in_bounds;
+#else
+  (void)in_bounds;
+  (void)status;
+  return true;
+#endif
+}
 
 // Everything a kernel of this library needs, by value.
 struct AttnParams {

@@ -309,6 +309,10 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
     if (i >= s.len_q || s.len_k == 0) continue;  // no tile reads this row
     const size_t row = static_cast<size_t>(r);
     const size_t t0 = tiled_index(p, b, i, 0);   // + h * 128 for head h
+    if (!bounds_ok(t0 + static_cast<size_t>(p.hq - 1) * kBlockM <
+                       static_cast<size_t>(p.pair_cap_q) * p.hq * kBlockM,
+                   p.header + kHdrStatus))
+      continue;
     for (int h = lane; h < p.hq; h += 32)
       p.lse_t[t0 + static_cast<size_t>(h) * kBlockM] = p.lse_in[row * p.hq + h] * kLog2e;
     const uint4* o = reinterpret_cast<const uint4*>(static_cast<const T*>(p.out_in) +

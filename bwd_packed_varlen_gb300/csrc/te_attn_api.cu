@@ -15,6 +15,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/te_attn.h"
 #include "common.cuh"
 #include "launch.h"
@@ -102,10 +104,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Shared argument checks of both entry points. Returns TE_OK or an error code.
 int check_common(int batch, int total_q, int total_kv, int hq, int hkv, int d, float attn_scale,
                  int mask_type, int dtype, const int32_t* cu_q, const int32_t* cu_kv,
-                 const int32_t* cu_q_pad, const int32_t* cu_kv_pad, const void* workspace) {
+                 const int32_t* cu_q_pad, const int32_t* cu_kv_pad) {
   if (!cu_q || !cu_kv || !cu_q_pad || !cu_kv_pad)
     return fail(TE_ERR_INVALID_ARG, "cu_seqlens pointers must not be NULL");
-  if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
   if (batch < 1) return fail(TE_ERR_INVALID_ARG, "batch must be >= 1");
   if (total_q < 0 || total_kv < 0) return fail(TE_ERR_INVALID_ARG, "total_q/total_kv must be >= 0");
   if (hq < 1 || hkv < 1) return fail(TE_ERR_INVALID_ARG, "hq and hkv must be >= 1");
@@ -172,10 +173,20 @@ std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRecord> g_prof;
 
-// Runs `launch` between two events on `st` when profiling is enabled.
+const char* const kKernelNames[TE_NUM_KERNELS] = {"teattn schedule", "teattn forward",
+                                                   "teattn zero fill", "teattn delta",
+                                                   "teattn dK/dV", "teattn dQ",
+                                                   "teattn widen e4m3"};
+
+// Runs `launch` between two events on `st` when profiling is enabled, inside an
+// NVTX range named after the kernel (visible to Nsight tools; a no-op without one).
 template <typename F>
 cudaError_t timed(int kernel, cudaStream_t st, F&& launch) {
   if (!g_prof_on) return launch();
+  struct Range {
+    explicit Range(const char* n) { nvtxRangePushA(n); }
+    ~Range() { nvtxRangePop(); }
+  } range(kKernelNames[kernel]);
   ProfRecord r{kernel, nullptr, nullptr};
   cudaError_t e = cudaEventCreate(&r.start);
   if (e == cudaSuccess) e = cudaEventCreate(&r.stop);
@@ -199,7 +210,7 @@ void set_last_error(const std::string& msg) { g_last_error = msg; }
 
 extern "C" {
 
-int te_attn_version(void) { return 10000; }
+int te_attn_version(void) { return 10100; }
 
 size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
   (void)hkv;
@@ -236,9 +247,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
                     int dtype, void* workspace, size_t workspace_bytes, void* stream, bool sbhd,
                     E4m3Scales e4m3 = E4m3Scales{false, 1.f, 1.f, 1.f}) {
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
-                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
-                        workspace);
+                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded);
   if (rc != TE_OK) return rc;
+  if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
   if (total_q > 0 && (!q || !out || !lse))
     return fail(TE_ERR_INVALID_ARG, "q, out and lse must not be NULL");
   if (total_kv > 0 && (!k || !v)) return fail(TE_ERR_INVALID_ARG, "k and v must not be NULL");
@@ -283,8 +294,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* out, floa
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   if (e4m3.on && total_kv > 0) {
     // every row of V, pad slots included (they are finite e4m3 values)
-    e = teattn::launch_widen_e4m3(v, ws + L.total, static_cast<size_t>(total_kv) * hkv * d, e4m3.v,
-                                  sms, st);
+    e = timed(TE_KERNEL_WIDEN, st, [&] {
+      return teattn::launch_widen_e4m3(v, ws + L.total, static_cast<size_t>(total_kv) * hkv * d,
+                                       e4m3.v, sms, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "widen V");
   }
   if (total_q > 0 && total_kv > 0) {
@@ -356,16 +369,19 @@ int te_attn_fwd_thd_e4m3(const void* q, const void* k, const void* v, void* out,
                   E4m3Scales{true, q_descale, k_descale, v_descale});
 }
 
-static int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,
-                    const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
-                    const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
-                    const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
-                    int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
-                    void* workspace, size_t workspace_bytes, void* stream, cudaEvent_t dq_done,
-                    bool sbhd) {
+}  // extern "C"
+
+namespace teattn {
+// Every host-side check of a backward call except the workspace ones: TE_OK or the
+// error code (with the message for te_attn_last_error()).
+int bwd_check_args(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                   const float* lse, const void* dq, const void* dk, const void* dv,
+                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                   const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                   int batch, int total_q, int total_kv, int hq, int hkv, int d, float attn_scale,
+                   int mask_type, int dtype) {
   int rc = check_common(batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type, dtype,
-                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
-                        workspace);
+                        cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded);
   if (rc != TE_OK) return rc;
   if (total_q > 0 && (!q || !out || !dout || !lse || !dq))
     return fail(TE_ERR_INVALID_ARG, "q, out, dout, lse and dq must not be NULL");
@@ -374,6 +390,27 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   const void* ptrs[] = {q, k, v, out, dout, dq, dk, dv};
   for (const void* x : ptrs)
     if (x && !aligned16(x)) return fail(TE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  Layout L;
+  if (!make_layout(batch, total_q, total_kv, hq, true, &L))
+    return fail(TE_ERR_INVALID_ARG, "sizes out of range");
+  return TE_OK;
+}
+}  // namespace teattn
+
+extern "C" {
+
+static int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                    const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
+                    int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream, cudaEvent_t dq_done,
+                    bool sbhd) {
+  int rc = teattn::bwd_check_args(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv,
+                                  cu_seqlens_q_padded, cu_seqlens_kv_padded, batch, total_q,
+                                  total_kv, hq, hkv, d, attn_scale, mask_type, dtype);
+  if (rc != TE_OK) return rc;
+  if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
   Layout L;
   if (!make_layout(batch, total_q, total_kv, hq, true, &L))
     return fail(TE_ERR_INVALID_ARG, "sizes out of range");

@@ -93,9 +93,23 @@ extern "C" {
 #define TE_ERR_BAD_SEQLENS (-5)
 #define TE_ERR_TIMEOUT (-6)
 
-/* Device status bits reported by te_attn_read_status(). */
+/*
+ * Device status bits reported by te_attn_read_status():
+ *   TE_STATUS_BAD_SEQLENS   cu_seqlens inconsistent with the tensor extents (a real
+ *                           length above its padded one, offsets past the tensor);
+ *                           the offending sequences are treated as empty.
+ *   TE_STATUS_TIMEOUT       a pipeline wait inside a kernel ran past its limit (4 s);
+ *                           every other wait of that kernel then gave up too, the
+ *                           kernel freed its tensor memory and returned, and the
+ *                           outputs of the call are undefined.
+ *   TE_STATUS_OUT_OF_BOUNDS only in the debug build of the library (compiled with
+ *                           TEATTN_DEBUG_BOUNDS, libteattn_debug.so): a computed
+ *                           global offset fell outside its buffer; the access was
+ *                           skipped. The release build does not check.
+ */
 #define TE_STATUS_BAD_SEQLENS 1
 #define TE_STATUS_TIMEOUT 2
+#define TE_STATUS_OUT_OF_BOUNDS 4
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int te_attn_version(void);
@@ -217,6 +231,24 @@ int te_attn_fwd_thd_e4m3(const void* q, const void* k, const void* v, void* out,
 int te_attn_read_status(const void* workspace, int* status, void* stream);
 
 /*
+ * Self-test of the bounded-wait unwind path (no counterpart in the pages; a test and
+ * debugging aid). Launches one block on `stream` that allocates all of its SM's
+ * tensor memory, waits with a limit of `limit_us` microseconds (1 .. 1000000) on a
+ * barrier no thread ever arrives on, while a second warp waits with the library's
+ * default limit on a barrier the first would release. The first wait runs out and
+ * records TE_STATUS_TIMEOUT in the status word of `workspace` (at least 256 bytes);
+ * the second sees the bit and gives up early; the block frees its tensor memory and
+ * returns. Afterwards te_attn_read_status(workspace) reports TE_STATUS_TIMEOUT and
+ * header words 8..11 of the workspace hold: the first wait's result (0 = timed out),
+ * its duration and the second wait's duration in microseconds, and 1 once the block
+ * reached its end. The GPU context stays usable; a later call that uses the same
+ * workspace rewrites the status word. Returns TE_OK, TE_ERR_INVALID_ARG,
+ * TE_ERR_WORKSPACE_TOO_SMALL or TE_ERR_CUDA (launch failure).
+ */
+int te_attn_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                  unsigned int limit_us, void* stream);
+
+/*
  * Kernel timing (profiling aid). te_attn_profile_enable(1) makes every later call
  * bracket each of its kernel launches with a pair of CUDA events recorded on the
  * call's stream; te_attn_profile_read() synchronises on those events, adds each
@@ -232,7 +264,8 @@ int te_attn_read_status(const void* workspace, int* status, void* stream);
 #define TE_KERNEL_DELTA 3
 #define TE_KERNEL_DKDV 4
 #define TE_KERNEL_DQ 5
-#define TE_NUM_KERNELS 6
+#define TE_KERNEL_WIDEN 6
+#define TE_NUM_KERNELS 7
 int te_attn_profile_enable(int enable);
 int te_attn_profile_read(double* total_ms, int* launches);
 
@@ -247,14 +280,19 @@ int te_attn_profile_read(double* total_ms, int* launches);
  * the library (a __device__ array: every GPU that loads it keeps it until the
  * process exits). It calls no cudaMalloc, cudaFree or other allocating routine.
  * - The first call on a device looks up the array's device address with that
- *   device current and caches it; make that first call before any stream capture.
+ *   device current and caches it with the identity of the current CUDA context (a
+ *   call in another context, e.g. after cudaDeviceReset, looks it up again); make
+ *   that first call before any stream capture.
  * - All calls on a device share the one array and it keeps the last call's
  *   contents; nothing in it needs to start at zero (each call rewrites what it
  *   reads), but calls that overlap on the GPU race on it: order them (one stream,
  *   or events).
- * - Returns TE_ERR_WORKSPACE_TOO_SMALL (and a message naming the size needed) when
- *   te_attn_bwd_workspace_size() of the problem exceeds the array; otherwise the
- *   same results and errors as te_attn_bwd_thd.
+ * - Arguments are checked first, with the codes and messages of te_attn_bwd_thd;
+ *   then TE_ERR_WORKSPACE_TOO_SMALL (and a message naming the size needed) is
+ *   returned when te_attn_bwd_workspace_size() of the problem exceeds the array.
+ *   Otherwise the results are those of te_attn_bwd_thd, bit for bit.
+ * - Device-side errors (TE_STATUS_* bits) land in the array's status word:
+ *   te_attn_read_status_noalloc() reads them for the current device.
  */
 #define TE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int te_attn_bwd_thd_noalloc(const void* q, const void* k, const void* v, const void* out,
@@ -264,6 +302,13 @@ int te_attn_bwd_thd_noalloc(const void* q, const void* k, const void* v, const v
                             const int32_t* cu_seqlens_kv_padded, int batch, int total_q,
                             int total_kv, int max_seqlen_q, int max_seqlen_kv, int hq, int hkv,
                             int d, float attn_scale, int mask_type, int dtype, void* stream);
+
+/*
+ * The status word of the last te_attn_bwd_thd_noalloc call on the current device
+ * (as te_attn_read_status() gives it for a workspace): synchronises `stream`, then
+ * copies the word into *status. Returns TE_OK, TE_ERR_INVALID_ARG or TE_ERR_CUDA.
+ */
+int te_attn_read_status_noalloc(int* status, void* stream);
 
 /* Thread-local description of the last error returned on this thread. */
 const char* te_attn_last_error(void);

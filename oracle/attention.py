@@ -288,8 +288,10 @@ def attn_fwd_thd_e4m3(q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens_q,
     :func:`attn_fwd_thd` does. The pages give no FP8 arithmetic beyond [2892]'s
     failing forward with real != padded lengths; the per-tensor factors are this
     package's reading. Returns ``(out, lse)`` float64.
-    Parity: pinned through :func:`attn_fwd_thd` (the e4m3 decoding it relies on is
-    pinned against the format's definition in the tests)."""
+    Parity: pinned by the one-key closed form (out = v8 * v_descale, lse =
+    attn_scale * q_descale * k_descale * <q8, k8>) and through :func:`attn_fwd_thd`;
+    the e4m3 decoding it relies on is pinned code by code against the format's
+    definition in the tests."""
     q = np.asarray(q8, dtype=np.float64) * float(q_descale)
     k = np.asarray(k8, dtype=np.float64) * float(k_descale)
     v = np.asarray(v8, dtype=np.float64) * float(v_descale)
@@ -377,7 +379,9 @@ def fwd_bwd_flops(cu_seqlens_q, cu_seqlens_kv, hq, d, mask_type):
 
     Per (sequence, query head): ``F_fwd = 4 d pairs`` with ``pairs = Lq Lk``
     (padding) or ``Lq Lk / 2`` (either causal alignment); forward + backward is ``3.5 F_fwd``
-    (2 GEMMs forward, 5 backward)."""
+    (2 GEMMs forward, 5 backward).
+    Parity: pinned against a brute-force count of the kept entries of the score
+    matrices."""
     causal = _is_causal(mask_type)
     lq = np.diff(np.asarray(cu_seqlens_q, dtype=np.int64)).astype(np.float64)
     lk = np.diff(np.asarray(cu_seqlens_kv, dtype=np.int64)).astype(np.float64)

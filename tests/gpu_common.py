@@ -14,6 +14,18 @@ import oracle
 REL_TOL = 1e-2
 COS_TOL = 0.9999
 LSE_TOL = 1e-3
+# Row by row and element by element (a row is one token's d values of one head):
+#   |x_r - ref_r|   <= ROW_TOL  * (|ref_r| + rms)      for every row r,
+#   |x_e - ref_e|   <= ELEM_TOL * (|ref_e| + (|ref_r| + rms) / sqrt(d)) for every element,
+# rms = root-mean-square norm of the reference's nonzero rows. ROW_TOL is 8 bf16
+# unit roundoffs (8 * 2^-8): the 16-bit roundings a row goes through (P or dS before
+# the second product, the output, and D from the stored output) each add at most
+# one unit relative to the row's scale; the rms term keeps rows that are small
+# because of cancellation (dQ rows sum dS_ij K_j with sum_j dS_ij = 0) on the
+# tensor's scale. ELEM_TOL adds the same allowance per element on the element's
+# own size plus its row's typical element size.
+ROW_TOL = 8.0 * 2.0 ** -8
+ELEM_TOL = 8.0 * 2.0 ** -8
 
 
 def to_dev(w, dev="cuda"):
@@ -57,9 +69,41 @@ def rel_cos(a, b):
     return float(np.linalg.norm(a - b) / nb), float(a @ b / (na * nb)) if na > 0 else 0.0
 
 
+def row_elem_check(got, ref):
+    """Worst row and element ratios to their bounds (<= 1 passes); see ROW_TOL."""
+    a = np.asarray(got, dtype=np.float64)
+    b = np.asarray(ref, dtype=np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    d = b.shape[-1]
+    a2, b2 = a.reshape(-1, d), b.reshape(-1, d)
+    rn = np.linalg.norm(b2, axis=1)
+    nz = rn > 0
+    rms = float(np.sqrt(np.mean(rn[nz] ** 2))) if nz.any() else 0.0
+    err = np.linalg.norm(a2 - b2, axis=1)
+    row_bound = ROW_TOL * (rn + rms)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        row_ratio = np.where(row_bound > 0, err / row_bound, np.where(err > 0, np.inf, 0.0))
+        elem_bound = ELEM_TOL * (np.abs(b2) + ((rn + rms) / np.sqrt(d))[:, None])
+        ediff = np.abs(a2 - b2)
+        elem_ratio = np.where(elem_bound > 0, ediff / elem_bound, np.where(ediff > 0, np.inf, 0.0))
+    r = int(np.argmax(row_ratio)) if row_ratio.size else 0
+    e = np.unravel_index(int(np.argmax(elem_ratio)), elem_ratio.shape) if elem_ratio.size else (0, 0)
+    return {"row_ratio": float(row_ratio.max()) if row_ratio.size else 0.0, "row": r,
+            "row_err": float(err[r]) if err.size else 0.0, "row_norm": float(rn[r]) if rn.size else 0.0,
+            "elem_ratio": float(elem_ratio.max()) if elem_ratio.size else 0.0,
+            "elem": tuple(int(x) for x in e), "rms": rms}
+
+
 def assert_close(name, got, ref):
+    """Whole tensor (rel. Frobenius, cosine), then every row and every element."""
     rel, cos = rel_cos(got, ref)
     assert rel <= REL_TOL and cos >= COS_TOL, f"{name}: rel={rel:.3e} cos={cos:.6f}"
+    m = row_elem_check(got, ref)
+    assert m["row_ratio"] <= 1.0, (
+        f"{name}: row {m['row']} error {m['row_err']:.3e} exceeds {ROW_TOL:.3g} * (|ref_r| "
+        f"{m['row_norm']:.3e} + rms {m['rms']:.3e}) by {m['row_ratio']:.2f}x")
+    assert m["elem_ratio"] <= 1.0, (
+        f"{name}: element {m['elem']} exceeds its bound by {m['elem_ratio']:.2f}x")
     return rel, cos
 
 

@@ -147,3 +147,44 @@ def test_host_checked_errors_launch_nothing(lib):
                                 P, big, None) == -1  # negative length
     assert lib.te_attn_fwd_sbhd(P, P, P, P, P, cu, cu, 2, 1 << 30, 8, 4, 2, 64, 0.1, 1, 1, P, big,
                                 None) == -1       # rows overflow int
+
+
+def test_debug_build_exports_the_same_symbols(lib):
+    """The bounds-checking build exports every declared function too."""
+    import bwd_packed_varlen_gb300 as ta
+    dbg = ta.library(debug=True)
+    for name in _declared():
+        assert hasattr(dbg, name), name
+    assert dbg.te_attn_version() == lib.te_attn_version()
+
+
+def test_noalloc_checks_arguments_before_sizes(lib):
+    """te_attn_bwd_thd_noalloc answers a bad argument with te_attn_bwd_thd's own code
+    and message, before it compares the problem with its built-in scratch size, and
+    launches nothing in either case (placeholder pointers, no GPU needed)."""
+    P = ctypes.c_void_p(1 << 20)
+    cu = ctypes.c_void_p(1 << 21)
+
+    def call(batch=2, tq=64, tk=64, hq=4, hkv=2, d=64, mask=1, dtype=1, lse=P):
+        return lib.te_attn_bwd_thd_noalloc(P, P, P, P, P, lse, P, P, P, cu, cu, cu, cu, batch, tq,
+                                           tk, 0, 0, hq, hkv, d, 0.1, mask, dtype, None)
+    huge = 1 << 22  # a problem whose workspace exceeds the built-in scratch
+    assert call(tq=huge, hq=3) == -1                  # hq not a multiple of hkv wins
+    assert b"multiple of hkv" in lib.te_attn_last_error()
+    assert call(tq=huge, d=12) == -2                  # unsupported head dim wins
+    assert call(tq=huge, batch=0) == -1
+    assert call(tq=huge, mask=9) == -2
+    assert call(tq=huge, lse=None) == -1              # NULL lse
+    assert call(tq=huge) == -3                        # valid arguments, too large
+    assert b"more than the built-in" in lib.te_attn_last_error()
+
+
+def test_selftest_and_status_reads_check_arguments(lib):
+    """Host-side argument errors of the self-test and status entry points (no launch)."""
+    assert lib.te_attn_selftest_wait_timeout(None, 256, 10, None) == -1
+    P = ctypes.c_void_p(1 << 20)
+    assert lib.te_attn_selftest_wait_timeout(P, 64, 10, None) == -3
+    assert lib.te_attn_selftest_wait_timeout(P, 256, 0, None) == -1
+    assert lib.te_attn_selftest_wait_timeout(P, 256, 2_000_000, None) == -1
+    assert lib.te_attn_read_status_noalloc(None, None) == -1
+    assert lib.te_attn_read_status(None, None, None) == -1

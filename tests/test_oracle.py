@@ -470,6 +470,58 @@ def test_e4m3_forward_is_the_dequantised_forward():
         assert np.array_equal(x, y)
 
 
+def test_e4m3_forward_single_key_closed_form():
+    """Closed form of the e4m3 forward with one key per sequence: every query sees
+    only key 0, so P = 1, out = v8 * v_descale and
+    lse = attn_scale * q_descale * k_descale * <q8, k8>. Distinct descale factors
+    make a swapped factor (v's in place of q's or k's), a factor applied twice or
+    a missing attn_scale fail."""
+    rng = np.random.default_rng(77)
+    lq = [3, 5]
+    cu_q = np.array([0, 3, 8])
+    cp_q = np.array([0, 4, 10])
+    cu_k = np.array([0, 1, 2])
+    cp_k = np.array([0, 2, 3])
+    hq, hkv, d = 4, 2, 16
+    q8 = np.round(rng.standard_normal((10, hq, d)) * 4) / 4
+    k8 = np.round(rng.standard_normal((3, hkv, d)) * 4) / 4
+    v8 = np.round(rng.standard_normal((3, hkv, d)) * 4) / 4
+    qd, kd, vd, sc = 0.5, 0.125, 3.0, 0.7
+    for mask in (MASK_PADDING, MASK_PADDING_CAUSAL):
+        out, lse = oracle.attn_fwd_thd_e4m3(q8, k8, v8, qd, kd, vd, cu_q, cu_k, cp_q, cp_k, sc, mask)
+        for b in range(2):
+            for i in range(lq[b]):
+                r = cp_q[b] + i
+                for h in range(hq):
+                    g = h // (hq // hkv)
+                    kr = cp_k[b]
+                    assert np.allclose(out[r, h], v8[kr, g] * vd, rtol=0, atol=1e-12)
+                    want = sc * qd * kd * float(q8[r, h] @ k8[kr, g])
+                    assert abs(lse[r, h] - want) <= 1e-12 * max(1.0, abs(want))
+        assert np.all(out[3] == 0) and np.all(lse[3] == 0)  # pad slot of sequence 0
+
+
+def test_flop_count_matches_the_mask():
+    """The metric's pair count against a brute-force count of the kept (query, key)
+    entries of the oracle's own score matrices: equal for the padding mask; for
+    either causal mask the convention Lq*Lk/2 sits below the exact triangle
+    count sum_i (keys of row i) by Lq/2 when Lq = Lk (it drops the diagonal's
+    half), so 3.5 * 4 * d * hq * (count - Lq/2) per sequence reproduces it."""
+    from oracle.attention import _scores, _is_causal
+    lens = [5, 9, 1, 16]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    hq, d = 3, 8
+    for mask in (MASK_PADDING, MASK_PADDING_CAUSAL, MASK_PADDING_CAUSAL_BOTTOM_RIGHT):
+        kept = 0.0
+        half_diag = 0.0
+        for L in lens:
+            s = _scores(np.ones((L, d)), np.ones((L, d)), 1.0, _is_causal(mask))
+            kept += float(np.isfinite(s).sum())
+            half_diag += L / 2.0 if mask != MASK_PADDING else 0.0
+        want = 3.5 * 4.0 * d * hq * (kept - half_diag)
+        assert oracle.fwd_bwd_flops(cu, cu, hq, d, mask) == want, mask
+
+
 def test_golden_issue2448_zero_rows():
     """[2448] 'Expected behavior': on the second call (query lengths 0 and 3)
     the first 4 tokens of dk and dv are all zero; on the first they are not."""
