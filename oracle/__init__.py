@@ -41,6 +41,8 @@ from .attention import (  # noqa: F401
     seq_spans,
     attn_group_fwd_bwd,
     attn_group_bwd_given,
+    attn_group_error_scales,
+    attn_error_scales_thd,
     attn_fwd_thd,
     attn_bwd_thd,
     attn_fwd_bwd_thd,

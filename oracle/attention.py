@@ -189,6 +189,92 @@ def attn_group_bwd_given(qg, kg, vg, outg, dog, lseg, scale, causal):
     return dq, dk, dv
 
 
+def attn_group_error_scales(qg, kg, vg, dog, scale, causal, norm=1):
+    """Magnitude sums that bound the rounding error of each output element of one
+    sequence and key/value group (test helper for the GPU comparisons).
+
+    An implementation that rounds a product's operand to 16 bits (P before P V and
+    P^T dO, dS before dS K and dS^T Q) changes the product by at most u times the
+    sum of the absolute values of its terms; one that forms D = rowsum(dout * out)
+    from a rounded ``out`` changes D_i by at most u a_i, and with it dS_ij by
+    P_ij u a_i. With ``norm=1`` (worst case) this returns, in float64 and the shapes
+    of :func:`attn_group_fwd_bwd`'s outputs:
+      m_out = |P| |V|
+      m_dq  = scale (|dS| |K| + (P * a) |K|)
+      m_dk  = scale sum_h (|dS|^T |Q| + (P * a)^T |Q|)
+      m_dv  = sum_h |P|^T |dout|
+    with a_i = sum_c |dout_ic| (|out_ic| + m_out_ic). With ``norm=2`` the terms of
+    each sum are combined as a root of the sum of squares instead (the size of a sum
+    of independent rounding errors), except that the D term of a dq row stays
+    |a_i| (P |K|): one D_i perturbs every term of that row alike. The products are
+    the same ones :func:`attn_group_fwd_bwd` forms, on absolute values.
+    Parity: pinned (norm=1 equals the plain products on nonnegative data and bounds
+    them from above elementwise; norm=2 lies between the largest term and norm=1)."""
+    if norm not in (1, 2):
+        raise ValueError("norm must be 1 or 2")
+    qg = np.asarray(qg, dtype=np.float64)
+    kg = np.asarray(kg, dtype=np.float64)
+    vg = np.asarray(vg, dtype=np.float64)
+    dog = np.asarray(dog, dtype=np.float64)
+    lq, G, d = qg.shape
+    lk = kg.shape[0]
+    m_out = np.zeros((lq, G, d))
+    m_dq = np.zeros((lq, G, d))
+    m_dk = np.zeros((lk, d))
+    m_dv = np.zeros((lk, d))
+    if lq == 0 or lk == 0:
+        return m_out, m_dq, m_dk, m_dv
+    pw = (lambda x: np.abs(x)) if norm == 1 else (lambda x: x * x)  # per-term power
+    root = (lambda x: x) if norm == 1 else np.sqrt
+    ak, av = pw(kg), pw(vg)
+    for j in range(G):
+        s = _scores(qg[:, j, :], kg, scale, causal)
+        p, _ = _softmax_rows(s)
+        do = dog[:, j, :]
+        out = p @ vg
+        dp = do @ vg.T
+        ds = p * (dp - (p * dp).sum(axis=1)[:, None])
+        mo = root(pw(p) @ av)
+        m_out[:, j, :] = mo
+        a = root(pw(do * (np.abs(out) + mo)).sum(axis=1))
+        pa = p * a[:, None]
+        d_term = pa @ np.abs(kg)  # one D_i moves the whole row alike
+        m_dq[:, j, :] = scale * (root(pw(ds) @ ak) + d_term)
+        aq = pw(qg[:, j, :])
+        m_dk += pw(scale) * (pw(ds).T @ aq + pw(pa).T @ aq)
+        m_dv += pw(p).T @ pw(do)
+    if norm == 2:
+        m_dk = np.sqrt(m_dk)
+        m_dv = np.sqrt(m_dv)
+    return m_out, m_dq, m_dk, m_dv
+
+
+def attn_error_scales_thd(q, k, v, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                          cu_seqlens_kv_padded, attn_scale, mask_type, norm=1):
+    """:func:`attn_group_error_scales` over packed sequences: ``(m_out, m_dq, m_dk,
+    m_dv)`` in the padded layout of ``(out, dq, dk, dv)``, 0 on rows that are not
+    computed; ``norm`` as there. Parity: pinned with :func:`attn_group_error_scales`."""
+    causal = _is_causal(mask_type)
+    hq, hkv, G = _check_heads(q, k)
+    qs = seq_spans(cu_seqlens_q, cu_seqlens_q_padded)
+    ks = seq_spans(cu_seqlens_kv, cu_seqlens_kv_padded)
+    Tq, _, d = q.shape
+    Tk = k.shape[0]
+    res = [np.zeros((Tq, hq, d)), np.zeros((Tq, hq, d)), np.zeros((Tk, hkv, d)),
+           np.zeros((Tk, hkv, d))]
+    for (oq, lq), (ok, lk) in zip(qs, ks):
+        for g in range(hkv):
+            hs = slice(g * G, (g + 1) * G)
+            mo, mq, mk, mv = attn_group_error_scales(
+                q[oq:oq + lq, hs], k[ok:ok + lk, g], v[ok:ok + lk, g], dout[oq:oq + lq, hs],
+                attn_scale, causal, norm)
+            res[0][oq:oq + lq, hs] = mo
+            res[1][oq:oq + lq, hs] = mq
+            res[2][ok:ok + lk, g] = mk
+            res[3][ok:ok + lk, g] = mv
+    return tuple(res)
+
+
 def _check_heads(q, k):
     hq, hkv = q.shape[1], k.shape[1]
     if hkv < 1 or hq % hkv != 0:

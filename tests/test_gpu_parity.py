@@ -16,8 +16,10 @@ import torch
 import oracle
 from bwd_packed_varlen_gb300 import workloads as W
 from gpu_common import (
+    UNIT_ROUNDOFF,
     assert_close,
     check_against_oracle,
+    error_scales,
     gpu_fwd_bwd,
     np64,
     oracle_fwd_bwd,
@@ -103,8 +105,9 @@ def test_backward_from_given_out_lse(name):
     t = to_dev(w)
     dq, dk, dv = ta.bwd(t["q"], t["k"], t["v"], out.cuda(), t["dout"], lse.cuda(), t["cu_q"],
                         t["cu_kv"], t["cu_q_pad"], t["cu_kv_pad"], w.attn_scale, w.mask_type)
-    for nm, a, b in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
-        assert_close(nm, np64(a), b)
+    scales = error_scales(w)
+    for nm, a, b, m in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, scales[1:]):
+        assert_close(nm, np64(a), b, m, UNIT_ROUNDOFF[w.dtype])
 
 
 # ----------------------------------------------------------------- edge cases
@@ -320,12 +323,15 @@ def test_throughput_workload_sampled():
         k = np64(w.k[oq:oq + L, g])
         v = np64(w.v[oq:oq + L, g])
         do = np64(w.dout[oq:oq + L, hs])
-        r = oracle.attn_group_fwd_bwd(q, k, v, do, w.attn_scale, True)
-        assert_close(f"out[{b},{g}]", out[oq:oq + L, hs], r[0])
+        r = oracle.attn_group_fwd_bwd(q, k, v, do, w.attn_scale, "tl")
+        m = list(zip(*(oracle.attn_group_error_scales(q, k, v, do, w.attn_scale, "tl", norm=n)
+                       for n in (1, 2))))
+        u = UNIT_ROUNDOFF[w.dtype]
+        assert_close(f"out[{b},{g}]", out[oq:oq + L, hs], r[0], m[0], u)
         assert np.abs(lse[oq:oq + L, hs] - r[1]).max() <= 1e-3
-        assert_close(f"dq[{b},{g}]", dq[oq:oq + L, hs], r[2])
-        assert_close(f"dk[{b},{g}]", dk[oq:oq + L, g], r[3])
-        assert_close(f"dv[{b},{g}]", dv[oq:oq + L, g], r[4])
+        assert_close(f"dq[{b},{g}]", dq[oq:oq + L, hs], r[2], m[1], u)
+        assert_close(f"dk[{b},{g}]", dk[oq:oq + L, g], r[3], m[2], u)
+        assert_close(f"dv[{b},{g}]", dv[oq:oq + L, g], r[4], m[3], u)
 
 
 def test_issue3333_reference_norms_from_page_rng():

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from bwd_packed_varlen_gb300 import workloads as W
-from gpu_common import assert_close, LSE_TOL, np64
+from gpu_common import assert_close, LSE_TOL, np64, UNIT_ROUNDOFF
 
 pytestmark = pytest.mark.gpu
 
@@ -48,11 +48,29 @@ def _run(q, k, v, do, cu_q, cu_kv, scale, mask):
     return out, lse, dq, dk, dv
 
 
-def _check(res, ref, lq, lk):
+def _scales(q, k, v, do, cu_q, cu_kv, scale, mask):
+    """Oracle magnitude sums in the sequence-major layout: computed on the packed
+    view of the same values (batch entry b at rows b * S ..) and laid back out."""
+    S_q, B = q.shape[:2]
+    S_kv = k.shape[0]
+    packed = lambda x: np.ascontiguousarray(np.swapaxes(np64(x), 0, 1)).reshape((-1,) + tuple(x.shape[2:]))
+    cp_q, cp_k = np.arange(B + 1) * S_q, np.arange(B + 1) * S_kv
+    back = lambda x, S: np.swapaxes(x.reshape((B, S) + x.shape[1:]), 0, 1)
+    res = []
+    for norm in (1, 2):
+        m = oracle.attn_error_scales_thd(packed(q), packed(k), packed(v), packed(do),
+                                         cu_q.numpy(), cu_kv.numpy(), cp_q, cp_k, scale, mask,
+                                         norm=norm)
+        res.append((back(m[0], S_q), back(m[1], S_q), back(m[2], S_kv), back(m[3], S_kv)))
+    return list(zip(*res))
+
+
+def _check(res, ref, lq, lk, scales):
     out, lse, dq, dk, dv = (np64(x) for x in res)
-    for name, a, b in (("out", out, ref[0]), ("dq", dq, ref[2]), ("dk", dk, ref[3]),
-                       ("dv", dv, ref[4])):
-        assert_close(name, a, b)
+    u = UNIT_ROUNDOFF[res[0].dtype]
+    for name, a, b, m in zip(("out", "dq", "dk", "dv"), (out, dq, dk, dv),
+                             (ref[0], ref[2], ref[3], ref[4]), scales):
+        assert_close(name, a, b, m, u)
     fin = np.isfinite(ref[1])
     assert np.array_equal(np.isneginf(lse), np.isneginf(ref[1]))
     assert np.abs(lse[fin] - ref[1][fin]).max() <= LSE_TOL
@@ -74,7 +92,7 @@ def test_sbhd_matches_oracle(mask, d):
     res = _run(q, k, v, do, cu_q, cu_kv, scale, mask)
     ref = oracle.attn_fwd_bwd_sbhd(np64(q), np64(k), np64(v), np64(do), cu_q.numpy(),
                                    cu_kv.numpy(), scale, mask)
-    _check(res, ref, lq, lk)
+    _check(res, ref, lq, lk, _scales(q, k, v, do, cu_q, cu_kv, scale, mask))
 
 
 def test_sbhd_equals_packed_bitwise():
@@ -113,7 +131,8 @@ def test_issue3216_native_layout():
     res = _run(q, k, v, do, cu, cu, w.attn_scale, W.MASK_PADDING_CAUSAL)
     ref = oracle.attn_fwd_bwd_sbhd(np64(q), np64(k), np64(v), np64(do), cu.numpy(), cu.numpy(),
                                    w.attn_scale, W.MASK_PADDING_CAUSAL)
-    _check(res, ref, [S, S], [S, S])
+    _check(res, ref, [S, S], [S, S],
+           _scales(q, k, v, do, cu, cu, w.attn_scale, W.MASK_PADDING_CAUSAL))
 
 
 def test_autograd_sbhd():
