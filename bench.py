@@ -346,6 +346,22 @@ def measure_variants(ta, w, t, flops, fwd_flops, flush, dev, steps=20, warmup=5)
     ms = time_calls(sbhd_step, flush, steps, warmup)
     out["sbhd_fwd_bwd"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
                            "shape": f"[{S}, {B}, h, d] with the workload's real lengths"}
+    # A/B of the backward: the two-kernel path (separate dQ kernel recomputing S and
+    # dP), selected by a workspace of the minimum size, against the default.
+    Tq, hq, d = t["q"].shape
+    Tk, hkv, _ = t["k"].shape
+    o = torch.empty_like(t["q"])
+    l = torch.empty((Tq, hq), dtype=torch.float32, device=dev)
+    ta.fwd(t["q"], t["k"], t["v"], *cu, w.attn_scale, w.mask_type, out=o, lse=l)
+    g = [torch.empty_like(t[n]) for n in ("q", "k", "v")]
+    for name, size in (("bwd_default", ta.bwd_workspace_size(w.batch, Tq, Tk, hq, hkv, d)),
+                       ("bwd_two_kernel", ta.bwd_workspace_size_min(w.batch, Tq, Tk, hq, hkv, d))):
+        ws = torch.empty(size, dtype=torch.uint8, device=dev)
+        ms = time_calls(lambda: ta.bwd(t["q"], t["k"], t["v"], o, t["dout"], l, *cu, w.attn_scale,
+                                       w.mask_type, dq=g[0], dk=g[1], dv=g[2], workspace=ws),
+                        flush, steps, warmup)
+        out[name] = {"ms": ms, "tflops": 2.5 * fwd_flops / (ms * 1e-3) / 1e12,
+                     "workspace_bytes": size}
     return out
 
 
@@ -556,8 +572,10 @@ def run_ours(args, rank, world, local_rank):
 
     # ------------------------------------------------ roofline of the dominant kernel
     peaks = load_peaks()
-    credited = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 2.0 * d * pairs_h}
-    executed = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 6.0 * d * pairs_h}
+    credited = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 2.0 * d * pairs_h,
+                "bwd_fused": 10.0 * d * pairs_h}
+    executed = {"fwd": 4.0 * d * pairs_h, "dkdv": 8.0 * d * pairs_h, "dq": 6.0 * d * pairs_h,
+                "bwd_fused": 10.0 * d * pairs_h}
     kernels = {}
     for name, (tot, cnt) in kprof.items():
         if cnt == 0:
@@ -569,7 +587,8 @@ def run_ours(args, rank, world, local_rank):
             ent["tflops_credited"] = credited[name] / (avg * 1e-3) / 1e12
             ent["tflops_executed"] = executed[name] / (avg * 1e-3) / 1e12
         kernels[name] = ent
-    dom = max(("fwd", "dkdv", "dq"), key=lambda n: kernels.get(n, {}).get("total_ms", 0.0))
+    dom = max(("fwd", "dkdv", "dq", "bwd_fused"),
+              key=lambda n: kernels.get(n, {}).get("total_ms", 0.0))
     # The dominant kernel runs for a few ms at a time inside a step of a fraction of
     # a second of timed work: the burst figure is its denominator.
     peak = peaks["bf16_tflops"]
@@ -583,6 +602,12 @@ def run_ours(args, rank, world, local_rank):
         dbytes = 2 * Tq * hq * d * 2 + Tq * hq * 4
         kernels["delta"]["gbs"] = dbytes / (kernels["delta"]["avg_ms"] * 1e-3) / 1e9
         kernels["delta"]["hbm_frac"] = kernels["delta"]["gbs"] / peaks["hbm_gbs"]
+    if "dq_convert" in kernels:
+        # reads the fp32 accumulator of every real row and head, writes 16-bit dq
+        real = int(w.cu_seqlens_q[-1])
+        cbytes = real * hq * d * (4 + 2)
+        kernels["dq_convert"]["gbs"] = cbytes / (kernels["dq_convert"]["avg_ms"] * 1e-3) / 1e9
+        kernels["dq_convert"]["hbm_frac"] = kernels["dq_convert"]["gbs"] / peaks["hbm_gbs"]
 
     cpu = None
     if not args.no_cpu_baseline and world == 1 and args.workload == "throughput":

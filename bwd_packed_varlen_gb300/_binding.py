@@ -69,7 +69,8 @@ def library(debug: bool = None) -> ctypes.CDLL:
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.te_attn_version.restype = i32
     L.te_attn_version.argtypes = []
-    for name in ("te_attn_fwd_workspace_size", "te_attn_bwd_workspace_size"):
+    for name in ("te_attn_fwd_workspace_size", "te_attn_bwd_workspace_size",
+                 "te_attn_bwd_workspace_size_min"):
         fn = getattr(L, name)
         fn.restype = sz
         fn.argtypes = [i32] * 6
@@ -154,7 +155,13 @@ def fwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
 
 
 def bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
+    """Workspace bytes of the backward's fastest path (the fused one for d <= 128)."""
     return int(library().te_attn_bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d))
+
+
+def bwd_workspace_size_min(batch, total_q, total_kv, hq, hkv, d) -> int:
+    """Smallest workspace the backward accepts (it then runs the two-kernel path)."""
+    return int(library().te_attn_bwd_workspace_size_min(batch, total_q, total_kv, hq, hkv, d))
 
 
 def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
@@ -329,7 +336,8 @@ def read_status(workspace, stream=None) -> int:
     return int(val.value)
 
 
-KERNELS = ("schedule", "fwd", "zero_fill", "delta", "dkdv", "dq", "widen_e4m3")
+KERNELS = ("schedule", "fwd", "zero_fill", "delta", "dkdv", "dq", "widen_e4m3", "bwd_fused",
+           "dq_convert")
 
 
 def profile_enable(on: bool = True) -> None:

@@ -23,16 +23,21 @@ enum HeaderWord : int {
   kHdrNextDkdv = 4,
   kHdrNextDq = 5,
   kHdrNumFPairs = 6, // number of (sequence, 256-row query tile pair) items
+  kHdrNextFused = 7, // work counter of the fused backward kernel
   kHdrSelftest = 8,  // words 8..11: results of te_attn_selftest_wait_timeout
   kHdrWords = 64     // header size in int32 words (256 bytes, keeps alignment)
 };
 
 // Work lists the scheduler sorts for a call (the prefix sums are always built).
-constexpr int kListQ = 1, kListK = 2, kListF = 4;
+// kListKChain builds the key-tile list in the order the fused backward needs
+// (instead of kListK's cost order): sequences with more key tiles first, and within
+// a sequence the key tiles in descending order.
+constexpr int kListQ = 1, kListK = 2, kListF = 4, kListKChain = 8;
 
 constexpr int kStatusBadSeqlens = 1;
 constexpr int kStatusTimeout = 2;
 constexpr int kStatusOutOfBounds = 4;
+constexpr int kStatusInternal = 8;  // a kernel found its launch unusable (e.g. misaligned shared memory)
 
 // Bounds checks of computed global offsets. In the debug build of the library
 // (TEATTN_DEBUG_BOUNDS defined) a failed check records kStatusOutOfBounds in the
@@ -68,6 +73,12 @@ struct AttnParams {
   float* lse_t;
   float* delta_t;
   const int* pref_q;   // prefix sums of query tiles per sequence (scheduler output)
+  // Fused backward: fp32 dQ accumulator, one tile of dq_halves x 32 KB per
+  // (natural query tile pair, head), and one int semaphore per (pair, head)
+  // counting the key tiles that have added into that tile.
+  float* dq_acc;
+  int* dq_sem;
+  int dq_halves;
 
   const int* cu_q;
   const int* cu_kv;

@@ -20,5 +20,7 @@ cudaError_t launch_attn_fwd_pair(const AttnParams& p, bool bf16, int num_sms, cu
 cudaError_t launch_attn_fwd_pair_e4m3(const AttnParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_attn_bwd_fused(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_dq_convert(const AttnParams& p, bool bf16, int num_sms, cudaStream_t st);
 
 }  // namespace teattn

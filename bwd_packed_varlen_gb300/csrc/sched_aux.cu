@@ -29,6 +29,12 @@ namespace teattn {
 // first, ties by natural order, so a persistent grid takes the long items first.
 // Up to kSortCap pairs are sorted in shared memory; a longer list keeps its
 // natural order. The result depends only on the cu_seqlens values.
+// For the fused backward the key-tile list is built in chain order instead
+// (kListKChain): sequences with more key tiles first (ties: lower index), and
+// inside a sequence its key tiles in DESCENDING order -- the order in which that
+// kernel's blocks add into each dQ tile, so a block only ever waits on key tiles
+// claimed before its own. A list longer than kSortCap keeps the sequences in
+// natural order, still with each sequence's key tiles descending.
 constexpr int kSchedThreads = 1024;
 constexpr int kSortCap = 8192;
 
@@ -87,6 +93,54 @@ __device__ int f_pair_cost(const AttnParams& p, int b, int t) {
                     ? (visible_keys(s, 2 * t + 1, p.causal) + kBlockN - 1) / kBlockN
                     : 0;
   return a + c;
+}
+
+// Key tiles of sequence b in chain order: natural index i (sequence b, its j-th
+// key tile) stands for key tile pref[b+1] - 1 - j.
+__device__ __forceinline__ int2 chain_pair(const int* pref, int B, long long i) {
+  const int b = find_seq(pref, B, static_cast<int>(i));
+  return make_int2(b, pref[b + 1] - 1 - static_cast<int>(i - pref[b]));
+}
+
+__device__ void build_chain_list(const AttnParams& p, const int* pref, int n, int2* out,
+                                 uint64_t* keys) {
+  const int B = p.batch;
+  if (n > kSortCap) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = chain_pair(pref, B, i);
+    return;
+  }
+  int m = 1;
+  while (m < n) m <<= 1;
+  constexpr uint64_t kLow = (1ull << 40) - 1;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    uint64_t key = ~0ull;
+    if (i < n) {
+      const int b = find_seq(pref, B, i);
+      const int nk = min(pref[b + 1] - pref[b], 0xffffff);
+      key = (static_cast<uint64_t>(0xffffff - nk) << 40) | static_cast<uint64_t>(i);
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  for (int k = 2; k <= m; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = keys[i], c = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((a > c) == up) {
+            keys[i] = c;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    out[i] = chain_pair(pref, B, static_cast<long long>(keys[i] & kLow));
+  __syncthreads();
 }
 
 // kKind: 0 query tiles, 1 key tiles, 2 forward pairs of query tiles.
@@ -185,6 +239,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
   const int nf = min(carry_f, p.pair_cap_f);
   if (p.sched_lists & kListQ) build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
   if (p.sched_lists & kListK) build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
+  else if (p.sched_lists & kListKChain) build_chain_list(p, pref_k, nk, p.k_pairs, sort_keys);
   if (p.sched_lists & kListF) build_list<2>(p, pref_f, nf, p.f_pairs, sort_keys);
   if (threadIdx.x == 0) {
     int status = bad ? kStatusBadSeqlens : 0;
@@ -197,6 +252,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
     p.header[kHdrNextFwd] = 0;
     p.header[kHdrNextDkdv] = 0;
     p.header[kHdrNextDq] = 0;
+    p.header[kHdrNextFused] = 0;
   }
 }
 
@@ -265,6 +321,13 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(AttnParams p, int mode) 
       if (k_row_computed(p, r)) continue;
       zero_row(p.dk, r, kbytes);
       zero_row(p.dv, r, kbytes);
+    }
+    // fused backward: the per-(query tile, head) counters of key tiles added to dQ
+    if (p.dq_sem) {
+      const size_t n = static_cast<size_t>(p.pair_cap_q) * p.hq;
+      const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+      for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        p.dq_sem[i] = 0;
     }
   }
 }

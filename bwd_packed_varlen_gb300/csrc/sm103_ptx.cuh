@@ -115,6 +115,84 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Make async-proxy accesses to global memory (bulk copies and reductions) and
+// generic-proxy accesses on either side of this fence ordered with each other.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Bulk shared -> global copies and reductions (bulk-group completion)
+// ---------------------------------------------------------------------------
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gmem_dst)),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+// gmem[i] += smem[i] for `bytes` / 4 fp32 values, performed at the L2.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* gmem_dst, const void* smem_src,
+                                                    uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gmem_dst)),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk groups are complete (writes performed).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Global semaphores (one thread): acquire-load polling and release increments
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *sem == target (acquire). Gives up like mbar_wait: after
+// kWaitLimitNs, or as soon as another thread has recorded a timeout.
+__device__ __forceinline__ bool sem_wait_eq(const int* sem, int target, int* status) {
+  if (ld_acquire_gpu(sem) == target) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(40);
+    if (ld_acquire_gpu(sem) == target) return true;
+    if ((it & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(status) & kErrTimeout) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// 16-byte shared-memory store.
+__device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tiled mode, 4-D maps
 // ---------------------------------------------------------------------------

@@ -1,8 +1,11 @@
 // C ABI of libteattn.so (declared in include/te_attn.h): argument checks,
 // workspace layout and the launch sequence of each call.
 //
-//   forward : schedule -> attention forward -> zero fill (out, lse)
-//   backward: schedule -> D = rowsum(dO * O) -> dK/dV -> dQ -> zero fill (dq, dk, dv)
+//   forward : schedule -> attention forward -> zero fill of rows no tile writes
+//   backward: schedule -> zero fill -> D = rowsum(dO * O) -> then either
+//             fused dK/dV/dQ -> dQ conversion           (head_dim <= 128, full workspace)
+//             dQ -> dK/dV                               (head_dim 256, or a workspace of
+//                                                        te_attn_bwd_workspace_size_min)
 //
 // All launches go to the caller's stream; nothing is allocated and nothing is
 // kept between calls except per-device constants (SM count).
@@ -38,7 +41,8 @@ int ok_status() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t header, pref_q, pref_k, pref_f, q_pairs, k_pairs, f_pairs, lse_t, delta_t, total;
+  size_t header, pref_q, pref_k, pref_f, q_pairs, k_pairs, f_pairs, lse_t, delta_t, dq_acc, dq_sem,
+      total;
   int cap_q, cap_k, cap_f;
 };
 
@@ -52,7 +56,12 @@ struct Layout {
 //   f_pairs int2[cap_f]      sorted (sequence, 256-row query tile pair)
 //   lse_t   fp32[cap_q*hq*128] backward only: lse * log2(e), tile-major
 //   delta_t fp32[cap_q*hq*128] backward only: rowsum(dO * O), tile-major
-bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L) {
+//   dq_acc  fp32 tiles of dq_halves x 32 KB per (query tile pair, head), fused
+//           backward only: the ordered dQ accumulator
+//   dq_sem  int32[cap_q*hq]  fused backward only: key tiles added to each dQ tile
+// dq_halves: 0 (no fused backward), 1 (head_dim <= 64) or 2 (head_dim <= 128).
+bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L,
+                 int dq_halves = 0) {
   if (batch < 1 || total_q < 0 || total_kv < 0 || hq < 1) return false;
   // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
   const long long cq = static_cast<long long>(total_q) / teattn::kBlockM + batch + 1;
@@ -82,9 +91,16 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   if (backward) off = align_up(off + tiled, 256);
   L->delta_t = off;
   if (backward) off = align_up(off + tiled, 256);
+  L->dq_acc = off;
+  off += static_cast<size_t>(cq) * hq * dq_halves * 32768;
+  L->dq_sem = off;
+  if (dq_halves > 0) off = align_up(off + static_cast<size_t>(cq) * hq * sizeof(int), 256);
   L->total = off;
   return true;
 }
+
+// 64-column fp32 halves of a dQ tile in the fused backward (0: no fused path).
+int fused_halves(int d) { return d <= 64 ? 1 : (d <= 128 ? 2 : 0); }
 
 int num_sms_of_current_device() {
   static int cache[64] = {0};
@@ -176,7 +192,8 @@ std::vector<ProfRecord> g_prof;
 const char* const kKernelNames[TE_NUM_KERNELS] = {"teattn schedule", "teattn forward",
                                                    "teattn zero fill", "teattn delta",
                                                    "teattn dK/dV", "teattn dQ",
-                                                   "teattn widen e4m3"};
+                                                   "teattn widen e4m3", "teattn fused backward",
+                                                   "teattn dQ conversion"};
 
 // Runs `launch` between two events on `st` when profiling is enabled, inside an
 // NVTX range named after the kernel (visible to Nsight tools; a no-op without one).
@@ -220,6 +237,12 @@ size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
 }
 
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
+  (void)hkv;
+  Layout L;
+  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_halves(d)) ? L.total : 0;
+}
+
+size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
   (void)hkv;
   (void)d;
   Layout L;
@@ -411,11 +434,21 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
                                   total_kv, hq, hkv, d, attn_scale, mask_type, dtype);
   if (rc != TE_OK) return rc;
   if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
+  // The fused backward needs the dQ accumulator; a workspace of only the minimum
+  // size (or head_dim 256) takes the separate dQ kernel instead.
   Layout L;
-  if (!make_layout(batch, total_q, total_kv, hq, true, &L))
-    return fail(TE_ERR_INVALID_ARG, "sizes out of range");
-  if (workspace_bytes < L.total)
-    return fail(TE_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than te_attn_bwd_workspace_size()");
+  const int halves = fused_halves(d);
+  bool fused = false;
+  if (halves > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, halves) &&
+      workspace_bytes >= L.total) {
+    fused = true;
+  } else {
+    if (!make_layout(batch, total_q, total_kv, hq, true, &L))
+      return fail(TE_ERR_INVALID_ARG, "sizes out of range");
+    if (workspace_bytes < L.total)
+      return fail(TE_ERR_WORKSPACE_TOO_SMALL,
+                  "workspace smaller than te_attn_bwd_workspace_size_min()");
+  }
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return fail(TE_ERR_CUDA, "no CUDA device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -429,7 +462,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   p.q = q;
   p.k = k;
   p.v = v;
-  p.sched_lists = teattn::kListQ | teattn::kListK;
+  p.sched_lists = fused ? teattn::kListKChain : (teattn::kListQ | teattn::kListK);
   p.out_in = out;
   p.dout = dout;
   p.lse_in = lse;
@@ -439,6 +472,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   char* ws = static_cast<char*>(workspace);
   p.lse_t = reinterpret_cast<float*>(ws + L.lse_t);
   p.delta_t = reinterpret_cast<float*>(ws + L.delta_t);
+  if (fused) {
+    p.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+    p.dq_sem = reinterpret_cast<int*>(ws + L.dq_sem);
+    p.dq_halves = halves;
+  }
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   p.pref_q = pref_q;
   int* pref_k = reinterpret_cast<int*>(ws + L.pref_k);
@@ -452,6 +490,19 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   if (total_q > 0) {
     e = timed(TE_KERNEL_DELTA, st, [&] { return teattn::launch_delta(p, bf16, sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "delta");
+  }
+  if (fused) {
+    if (total_q > 0 && total_kv > 0) {
+      e = timed(TE_KERNEL_BWD_FUSED, st, [&] { return teattn::launch_attn_bwd_fused(p, bf16, sms, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "fused backward");
+      e = timed(TE_KERNEL_DQ_CONVERT, st, [&] { return teattn::launch_dq_convert(p, bf16, sms, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dQ conversion");
+    }
+    if (dq_done) {
+      e = cudaEventRecord(dq_done, st);
+      if (e != cudaSuccess) return cuda_fail(e, "dq event record");
+    }
+    return ok_status();
   }
   if (total_q > 0 && total_kv > 0) {
     e = timed(TE_KERNEL_DQ, st, [&] { return teattn::launch_attn_bwd_dq(p, bf16, sms, st); });

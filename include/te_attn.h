@@ -110,6 +110,9 @@ extern "C" {
 #define TE_STATUS_BAD_SEQLENS 1
 #define TE_STATUS_TIMEOUT 2
 #define TE_STATUS_OUT_OF_BOUNDS 4
+/* A kernel found its launch unusable (shared memory not 1024-byte aligned); it
+   returned without computing and the outputs of the call are undefined. */
+#define TE_STATUS_INTERNAL 8
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int te_attn_version(void);
@@ -118,9 +121,20 @@ int te_attn_version(void);
 size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
                                   int d);
 
-/* Bytes of workspace te_attn_bwd_thd needs for these sizes (0 on invalid sizes). */
+/*
+ * Bytes of workspace te_attn_bwd_thd needs for these sizes (0 on invalid sizes):
+ * with it, head dims up to 128 run the fused backward, whose dQ accumulator
+ * (fp32, one 128-row tile of 64 or 128 columns per query tile and head) is part of
+ * the workspace. te_attn_bwd_workspace_size_min() is the smallest workspace the
+ * backward accepts: with less than te_attn_bwd_workspace_size() bytes (and for
+ * d > 128 always) it runs the two-kernel path, a separate dQ kernel that
+ * recomputes the scores. Both paths are deterministic and meet the same tolerances;
+ * they are not bit-identical to each other (dQ is summed in a different order).
+ */
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
                                   int d);
+size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv,
+                                      int d);
 
 /*
  * Forward: writes out [total_q, hq, d] and lse [total_q, hq] (natural-log softmax
@@ -141,6 +155,10 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
  * heads of its group inside one thread block (no atomics). The arguments mirror
  * TransformerEngine's fused_attn_bwd as [2448] calls it (out and lse are
  * inputs; dropout 0; no bias; deterministic).
+ * Fused path (d <= 128, workspace of te_attn_bwd_workspace_size()): one kernel
+ * computes dK, dV and each key tile's share of dQ; the shares of a (query tile,
+ * head) are added into the fp32 accumulator in a fixed order (descending key
+ * tiles, ordered by a counter per tile), so dq is bit-identical from call to call.
  */
 int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -154,9 +172,10 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
 /*
  * Backward with a hand-over point (no counterpart in the pages): identical results
  * to te_attn_bwd_thd, plus `dq_done`, a cudaEvent_t created by the caller (or NULL),
- * is recorded on `stream` as soon as dq is final -- the backward computes dq before
- * dk and dv -- so that the caller can start consuming dq (a copy to the host, a
- * collective) on another stream while dk/dv are still being computed. Returns what
+ * is recorded on `stream` as soon as dq is final -- on the two-kernel path the
+ * backward computes dq before dk and dv, so that the caller can start consuming dq
+ * (a copy to the host, a collective) on another stream while dk/dv are still being
+ * computed; on the fused path dq, dk and dv become final together. Returns what
  * te_attn_bwd_thd returns, or TE_ERR_CUDA if the event cannot be recorded.
  */
 int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out,
@@ -265,7 +284,9 @@ int te_attn_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
 #define TE_KERNEL_DKDV 4
 #define TE_KERNEL_DQ 5
 #define TE_KERNEL_WIDEN 6
-#define TE_NUM_KERNELS 7
+#define TE_KERNEL_BWD_FUSED 7
+#define TE_KERNEL_DQ_CONVERT 8
+#define TE_NUM_KERNELS 9
 int te_attn_profile_enable(int enable);
 int te_attn_profile_read(double* total_ms, int* launches);
 
@@ -289,8 +310,10 @@ int te_attn_profile_read(double* total_ms, int* launches);
  *   or events).
  * - Arguments are checked first, with the codes and messages of te_attn_bwd_thd;
  *   then TE_ERR_WORKSPACE_TOO_SMALL (and a message naming the size needed) is
- *   returned when te_attn_bwd_workspace_size() of the problem exceeds the array.
- *   Otherwise the results are those of te_attn_bwd_thd, bit for bit.
+ *   returned when te_attn_bwd_workspace_size_min() of the problem exceeds the array.
+ *   Otherwise the results are those of te_attn_bwd_thd given a workspace of the
+ *   array's size, bit for bit: the fused path when te_attn_bwd_workspace_size() of
+ *   the problem fits in the array, the two-kernel path otherwise.
  * - Device-side errors (TE_STATUS_* bits) land in the array's status word:
  *   te_attn_read_status_noalloc() reads them for the current device.
  */
