@@ -205,12 +205,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       bool ok = true;
       int nxt = atomicAdd(p.header + kHdrNextFused, 1);
       for (; ok; ++ii) {
-        const int item = nxt < n_items ? nxt : -1;
+        int item = nxt < n_items ? nxt : -1;
+        Item I;
+        // The scheduler lists only key tiles some query sees, so every item has
+        // steps; one without (an inconsistent list) is passed over, never handed on.
+        while (item >= 0) {
+          I = decode(item);
+          if (I.steps > 0 && I.kt >= 0) break;
+          bounds_ok(false, status);  // recorded by the debug build
+          nxt = atomicAdd(p.header + kHdrNextFused, 1);
+          item = nxt < n_items ? nxt : -1;
+        }
         if (item < 0) {
           ok = ring_put(B.ring, ii, -1, status);
           break;
         }
-        const Item I = decode(item);
         if (!(ok = ring_put(B.ring, ii, item, status, I.steps))) break;
         nxt = atomicAdd(p.header + kHdrNextFused, 1);  // claimed now, handed over next
         if (ii > 0 && !(ok = mbar_wait(&B.kv_empty, (ii - 1) & 1, status))) break;

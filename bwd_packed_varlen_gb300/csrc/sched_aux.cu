@@ -96,10 +96,10 @@ __device__ int f_pair_cost(const AttnParams& p, int b, int t) {
 }
 
 // Key tiles of sequence b in chain order: natural index i (sequence b, its j-th
-// key tile) stands for key tile pref[b+1] - 1 - j.
+// key tile, j = i - pref[b]) stands for key tile nk_b - 1 - j = pref[b+1] - 1 - i.
 __device__ __forceinline__ int2 chain_pair(const int* pref, int B, long long i) {
   const int b = find_seq(pref, B, static_cast<int>(i));
-  return make_int2(b, pref[b + 1] - 1 - static_cast<int>(i - pref[b]));
+  return make_int2(b, pref[b + 1] - 1 - static_cast<int>(i));
 }
 
 __device__ void build_chain_list(const AttnParams& p, const int* pref, int n, int2* out,
