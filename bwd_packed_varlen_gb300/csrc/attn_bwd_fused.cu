@@ -40,9 +40,14 @@
 // of dK, dV and dQ); a TMA producer warp; an MMA warp (lane 0 issues every
 // tcgen05.mma); two reducer warps (lane 0) that add the staged dQ tiles of even and
 // odd steps to the accumulator with bulk reductions, so the compute warps never
-// wait on global memory. The compute warps stage dQ_t in shared memory that is
-// free once dQ_t is done: the dO buffer of the step (columns 0-63) and the dS tile
-// (columns 64-127).
+// wait on global memory. The compute warps stage dQ_t in the step's Q and dO
+// buffers (columns [0, kD/2) and [kD/2, kD) in fp32), which are free once dQ_t is
+// done: their last readers, dK_t and dV_t, ran before it. The producer refills the
+// stage once the reducer has read the staged tile, so a reducer has a whole step
+// to take its tile.
+// A block claims its next item only once it has issued the loads of its current
+// item's last step, so items start about in the order they are claimed and the key
+// tile a block waits on is normally already ahead of it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -79,7 +84,7 @@ struct FusedBars {
   uint64_t kv_full, kv_empty, acc_full, acc_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, y_free;
-  uint64_t stage_full[2], ds_free[2];
+  uint64_t stage_full[2];
   WorkRing ring;
   uint32_t tmem_slot;
 };
@@ -94,7 +99,6 @@ struct FusedShape {
   static constexpr int kTileBytes = kChunks * 16384;   // one 128-row K, V, Q or dO tile
   static constexpr int kStages = 2;                    // Q / dO stages
   static constexpr int kDSBytes = 32768;               // dS: 128 keys x 128 queries, 16-bit
-  static constexpr int kHalves = kD / 64;              // 64-column fp32 halves of a dQ tile
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
@@ -104,13 +108,15 @@ struct FusedShape {
   static constexpr int kOffDelta = kOffLse + kStages * kBM * 4;
   static constexpr int kOffBar = kOffDelta + kStages * kBM * 4;
   static constexpr int kSmemBytes = kOffBar + 1024;
+  // dQ staging: two halves of kD/2 fp32 columns, each exactly one Q or dO buffer
+  static constexpr int kHalfBytes = kBM * (kD / 2) * 4;
+  static constexpr int kHalfRowBytes = (kD / 2) * 4;
+  static_assert(kHalfBytes == kTileBytes, "a staging half fills one Q or dO buffer");
   static constexpr int kG = 32;                        // query columns per compute warp
   static constexpr int kOutCols = kD / 4;              // output columns per compute warp
   static constexpr uint32_t kColDK = 0, kColDV = 128, kColX = 256, kColY = 384;
   static_assert(sizeof(FusedBars) <= 1024, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  // the dO buffer of a step holds half a dQ tile in fp32 while it is staged
-  static_assert(kD == 64 || kTileBytes == 32768, "staging half in the dO buffer");
 };
 
 // TMEM column (relative to X) of the packed 16-bit operand for MMA k-step s (16
@@ -157,7 +163,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(&B.q_full[i], 1);
       mbar_init(&B.q_empty[i], 1);
       mbar_init(&B.stage_full[i], kFusedComputeWarps);
-      mbar_init(&B.ds_free[i], 1);
     }
     mbar_init(&B.s_full, 1);
     mbar_init(&B.dp_full, 1);
@@ -221,7 +226,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           break;
         }
         if (!(ok = ring_put(B.ring, ii, item, status, I.steps))) break;
-        nxt = atomicAdd(p.header + kHdrNextFused, 1);  // claimed now, handed over next
         if (ii > 0 && !(ok = mbar_wait(&B.kv_empty, (ii - 1) & 1, status))) break;
         mbar_arrive_expect_tx(&B.kv_full, 2 * S::kTileBytes);
         for (int c = 0; c < S::kChunks; ++c) {
@@ -245,6 +249,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           bulk_load(sLse + st * kBM, p.lse_t + ti, kBM * 4, &B.q_full[st]);
           bulk_load(sDelta + st * kBM, p.delta_t + ti, kBM * 4, &B.q_full[st]);
         }
+        if (!ok) break;
+        // claim the next item only now, close to when this block can start it
+        nxt = atomicAdd(p.header + kHdrNextFused, 1);
       }
     }
   } else if (warp == kFusedWarpMma) {
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (lane == 0) {
       int it = 0, ii = 0;
       bool ok = true;
-      constexpr uint32_t kHalfBytes = 32768;
+      constexpr uint32_t kHalfBytes = S::kHalfBytes;
       for (; ok; ++ii) {
         int steps = 0;
         const int item = ring_get(B.ring, ii, status, &ok, &steps);
@@ -353,23 +360,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const bool in_bounds = bounds_ok(
               rank >= 0 && tile < static_cast<size_t>(p.pair_cap_q) * p.hq, status);
           int* sem = p.dq_sem + (in_bounds ? tile : 0);
-          uint8_t* acc = reinterpret_cast<uint8_t*>(p.dq_acc) + (in_bounds ? tile : 0) * (S::kHalves * kHalfBytes);
+          uint8_t* acc = reinterpret_cast<uint8_t*>(p.dq_acc) + (in_bounds ? tile : 0) * (2 * kHalfBytes);
           if (in_bounds && rank > 0 && !(ok = sem_wait_eq(sem, rank, status))) break;
           fence_proxy_async_global();
           if (!(ok = mbar_wait(&B.stage_full[r], (it >> 1) & 1, status))) break;
-          const uint8_t* half0 = kD == 128 ? sDO + (it & 1) * S::kTileBytes : sDS;
+          const uint8_t* half0 = sQ + (it & 1) * S::kTileBytes;
+          const uint8_t* half1 = sDO + (it & 1) * S::kTileBytes;
           if (in_bounds) {
             if (rank == 0) {
               bulk_store(acc, half0, kHalfBytes);
-              if (kD == 128) bulk_store(acc + kHalfBytes, sDS, kHalfBytes);
+              bulk_store(acc + kHalfBytes, half1, kHalfBytes);
             } else {
               bulk_reduce_add_f32(acc, half0, kHalfBytes);
-              if (kD == 128) bulk_reduce_add_f32(acc + kHalfBytes, sDS, kHalfBytes);
+              bulk_reduce_add_f32(acc + kHalfBytes, half1, kHalfBytes);
             }
             bulk_commit();
             bulk_wait_read_all();
           }
-          mbar_arrive(&B.ds_free[r]);       // the dS tile may take the next step's dS
           mbar_arrive(&B.q_empty[it & 1]);  // the stage may take step it + 2
           if (in_bounds) {
             bulk_wait_all();
@@ -475,16 +482,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int k = 0; k < kG / 2; ++k) dd[k] = pack2<kBF16>(rr[2 * k], rr[2 * k + 1]);
         }
         tmem_st16(tmem + S::kColX + lane_base + col0 + 16, dd);
-        // The dS tile held the previous step's staged dQ columns: wait until its
-        // reducer has read them.
-        if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&B.ds_free[(it - 1) & 1], ((it - 1) >> 1) & 1, status));
-          if (!ok) break;
-        }
         {
-          // dS tile: row = key, 16-byte unit u of queries [8u, 8u+8) in 64-query
-          // chunks, 128-byte swizzled (unit ^ row % 8): K-major for dK's layout,
-          // MN-major (queries contiguous) as dQ's A operand.
+          // dS tile (its last reader, dQ of the previous step, is done): row = key,
+          // 16-byte unit u of queries [8u, 8u+8) in 64-query chunks, 128-byte
+          // swizzled (unit ^ row % 8) -- dQ's A operand, MN-major (queries contiguous).
           uint8_t* row = sDS + (grp >> 1) * 16384 + row_in_tile * 128;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -507,11 +508,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&B.y_free);
-          // fp32 staging, [128 rows][64 columns] per half, 256-byte rows, 16-byte
-          // unit u of a row stored at (u ^ row % 8): the accumulator's layout.
-          uint8_t* half = (kD == 128 && grp < 2) ? sDO + st * S::kTileBytes : sDS;
-          uint8_t* row = half + row_in_tile * 256;
-          const int u0 = kD == 128 ? 8 * (grp & 1) : 4 * grp;
+          // fp32 staging, [128 rows][kD/2 columns] per half (Q buffer: columns
+          // [0, kD/2), dO buffer: the rest), 16-byte unit u of a row stored at
+          // (u ^ row % 8): the accumulator's layout.
+          uint8_t* half = (grp < 2 ? sQ : sDO) + st * S::kTileBytes;
+          uint8_t* row = half + row_in_tile * S::kHalfRowBytes;
+          const int u0 = (grp & 1) * (S::kOutCols / 4);
 #pragma unroll
           for (int v = 0; v < S::kOutCols / 4; ++v)
             st_shared_v4(row + (((u0 + v) ^ sw) << 4), o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
@@ -566,7 +568,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(AttnParams p) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const bool causal = p.causal != 0;
-  const size_t tile_bytes = static_cast<size_t>(p.dq_halves) * 32768;
+  // tile: two halves of 128 rows x dq_cols/2 fp32 columns (dq_cols = 64 or 128)
+  const int half_units = p.dq_cols / 8;  // 16-byte units per row of a half
+  const size_t half_bytes = static_cast<size_t>(kBlockM) * half_units * 16;
+  const size_t tile_bytes = 2 * half_bytes;
   const int units = p.d / 4;  // 16-byte units of 4 fp32 per row and head
   using T = fused_elem_t<kBF16>;
   for (int r = gw; r < p.total_q; r += warps) {
@@ -580,9 +585,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(AttnParams p) {
     if (!bounds_ok(pair < static_cast<size_t>(p.pair_cap_q), p.header + kHdrStatus)) continue;
     for (int e = lane; e < p.hq * units; e += 32) {
       const int h = e / units, u = e % units;  // columns [4u, 4u+4) of head h
-      const int half = u >> 4, uu = u & 15;
+      const int half = u / half_units, uu = u % half_units;
       const uint8_t* tile = reinterpret_cast<const uint8_t*>(p.dq_acc) + (pair * p.hq + h) * tile_bytes;
-      const float4 v = *reinterpret_cast<const float4*>(tile + half * 32768 + ii * 256 + ((uu ^ (ii & 7)) << 4));
+      const float4 v = *reinterpret_cast<const float4*>(tile + half * half_bytes +
+                                                        static_cast<size_t>(ii) * half_units * 16 +
+                                                        ((uu ^ (ii & 7)) << 4));
       uint2 w;
       w.x = pack2<kBF16>(v.x * p.scale, v.y * p.scale);
       w.y = pack2<kBF16>(v.z * p.scale, v.w * p.scale);

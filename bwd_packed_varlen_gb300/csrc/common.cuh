@@ -73,12 +73,12 @@ struct AttnParams {
   float* lse_t;
   float* delta_t;
   const int* pref_q;   // prefix sums of query tiles per sequence (scheduler output)
-  // Fused backward: fp32 dQ accumulator, one tile of dq_halves x 32 KB per
-  // (natural query tile pair, head), and one int semaphore per (pair, head)
-  // counting the key tiles that have added into that tile.
+  // Fused backward: fp32 dQ accumulator, one 128-row tile of dq_cols (64 or 128)
+  // columns per (natural query tile pair, head), and one int semaphore per (pair,
+  // head) counting the key tiles that have added into that tile.
   float* dq_acc;
   int* dq_sem;
-  int dq_halves;
+  int dq_cols;
 
   const int* cu_q;
   const int* cu_kv;

@@ -56,12 +56,12 @@ struct Layout {
 //   f_pairs int2[cap_f]      sorted (sequence, 256-row query tile pair)
 //   lse_t   fp32[cap_q*hq*128] backward only: lse * log2(e), tile-major
 //   delta_t fp32[cap_q*hq*128] backward only: rowsum(dO * O), tile-major
-//   dq_acc  fp32 tiles of dq_halves x 32 KB per (query tile pair, head), fused
-//           backward only: the ordered dQ accumulator
+//   dq_acc  fp32[cap_q*hq*128*dq_cols] fused backward only: the ordered dQ
+//           accumulator, one 128-row tile per (query tile pair, head)
 //   dq_sem  int32[cap_q*hq]  fused backward only: key tiles added to each dQ tile
-// dq_halves: 0 (no fused backward), 1 (head_dim <= 64) or 2 (head_dim <= 128).
+// dq_cols: 0 (no fused backward), 64 (head_dim <= 64) or 128 (head_dim <= 128).
 bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L,
-                 int dq_halves = 0) {
+                 int dq_cols = 0) {
   if (batch < 1 || total_q < 0 || total_kv < 0 || hq < 1) return false;
   // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
   const long long cq = static_cast<long long>(total_q) / teattn::kBlockM + batch + 1;
@@ -92,15 +92,15 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   L->delta_t = off;
   if (backward) off = align_up(off + tiled, 256);
   L->dq_acc = off;
-  off += static_cast<size_t>(cq) * hq * dq_halves * 32768;
+  off += static_cast<size_t>(cq) * hq * teattn::kBlockM * dq_cols * sizeof(float);
   L->dq_sem = off;
-  if (dq_halves > 0) off = align_up(off + static_cast<size_t>(cq) * hq * sizeof(int), 256);
+  if (dq_cols > 0) off = align_up(off + static_cast<size_t>(cq) * hq * sizeof(int), 256);
   L->total = off;
   return true;
 }
 
-// 64-column fp32 halves of a dQ tile in the fused backward (0: no fused path).
-int fused_halves(int d) { return d <= 64 ? 1 : (d <= 128 ? 2 : 0); }
+// Columns of a dQ accumulator tile in the fused backward (0: no fused path).
+int fused_cols(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 0); }
 
 int num_sms_of_current_device() {
   static int cache[64] = {0};
@@ -239,7 +239,7 @@ size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
   (void)hkv;
   Layout L;
-  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_halves(d)) ? L.total : 0;
+  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_cols(d)) ? L.total : 0;
 }
 
 size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
@@ -437,9 +437,9 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   // The fused backward needs the dQ accumulator; a workspace of only the minimum
   // size (or head_dim 256) takes the separate dQ kernel instead.
   Layout L;
-  const int halves = fused_halves(d);
+  const int cols = fused_cols(d);
   bool fused = false;
-  if (halves > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, halves) &&
+  if (cols > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, cols) &&
       workspace_bytes >= L.total) {
     fused = true;
   } else {
@@ -475,7 +475,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   if (fused) {
     p.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
     p.dq_sem = reinterpret_cast<int*>(ws + L.dq_sem);
-    p.dq_halves = halves;
+    p.dq_cols = cols;
   }
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   p.pref_q = pref_q;
