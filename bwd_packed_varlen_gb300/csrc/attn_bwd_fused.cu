@@ -26,7 +26,8 @@
 // Why no wait can starve: items are claimed in list order from one counter
 // (every claim, including each block's first, is an atomic increment), and the
 // scheduler lists, within each (sequence, head group) chain, key tile kt + 1
-// before kt. A block waits only on contributions of key tile kt + 1 of its own
+// before kt (chain-major: a chain's key tiles are consecutive items, so they run
+// together and the dQ tiles they add to stay in L2). A block waits only on contributions of key tile kt + 1 of its own
 // chain, i.e. on items claimed before its own. Take the earliest-claimed item that
 // has not finished: the block that claimed it is working on it (its own earlier
 // items are finished, by the choice of item), and every item it waits on was
@@ -188,11 +189,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
   auto decode = [&](int item) {
     Item it;
-    const int2 pr = p.k_pairs[item / p.hkv];
-    it.g = item % p.hkv;
-    it.kt = pr.y;
-    it.b = pr.x;
-    it.s = load_seq(p, pr.x);
+    const int4 e = p.k_items[item];
+    it.b = e.x;
+    it.kt = e.y;
+    it.g = e.z;
+    it.s = load_seq(p, e.x);
     it.qt0 = first_query(it.s, it.kt * kBlockN, causal) / kBM;
     it.nq = (it.s.len_q + kBM - 1) / kBM;
     it.steps = G * (it.nq - it.qt0);

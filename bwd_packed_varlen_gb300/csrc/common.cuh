@@ -79,6 +79,10 @@ struct AttnParams {
   float* dq_acc;
   int* dq_sem;
   int dq_cols;
+  // Fused backward work items (sequence, key tile, kv head, 0) in chain-major
+  // order: for each sequence in the order of the chain-ordered key-tile list, each
+  // kv head, the sequence's key tiles from the last to the first.
+  int4* k_items;
 
   const int* cu_q;
   const int* cu_kv;

@@ -239,7 +239,23 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
   const int nf = min(carry_f, p.pair_cap_f);
   if (p.sched_lists & kListQ) build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
   if (p.sched_lists & kListK) build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
-  else if (p.sched_lists & kListKChain) build_chain_list(p, pref_k, nk, p.k_pairs, sort_keys);
+  else if (p.sched_lists & kListKChain) {
+    build_chain_list(p, pref_k, nk, p.k_pairs, sort_keys);
+    __syncthreads();
+    // Items of the fused backward, chain-major: sequence b's pairs occupy list
+    // positions [P, P + nk_b) (key tiles descending); its items are, per kv head g,
+    // those key tiles in the same order, at hkv * P + g * nk_b + (position - P).
+    // Running one (sequence, kv head) chain's key tiles together keeps the dQ tiles
+    // they all add to in L2.
+    for (int j = threadIdx.x; j < nk; j += blockDim.x) {
+      const int2 pr = p.k_pairs[j];
+      const int len = pref_k[pr.x + 1] - pref_k[pr.x];
+      const int start = j - (len - 1 - pr.y);
+      for (int g = 0; g < p.hkv; ++g)
+        p.k_items[static_cast<size_t>(start) * p.hkv + static_cast<size_t>(g) * len + (j - start)] =
+            make_int4(pr.x, pr.y, g, 0);
+    }
+  }
   if (p.sched_lists & kListF) build_list<2>(p, pref_f, nf, p.f_pairs, sort_keys);
   if (threadIdx.x == 0) {
     int status = bad ? kStatusBadSeqlens : 0;

@@ -42,7 +42,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
   size_t header, pref_q, pref_k, pref_f, q_pairs, k_pairs, f_pairs, lse_t, delta_t, dq_acc, dq_sem,
-      total;
+      k_items, total;
   int cap_q, cap_k, cap_f;
 };
 
@@ -59,9 +59,10 @@ struct Layout {
 //   dq_acc  fp32[cap_q*hq*128*dq_cols] fused backward only: the ordered dQ
 //           accumulator, one 128-row tile per (query tile pair, head)
 //   dq_sem  int32[cap_q*hq]  fused backward only: key tiles added to each dQ tile
+//   k_items int4[cap_k*hkv]  fused backward only: work items, chain-major
 // dq_cols: 0 (no fused backward), 64 (head_dim <= 64) or 128 (head_dim <= 128).
 bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, Layout* L,
-                 int dq_cols = 0) {
+                 int dq_cols = 0, int hkv = 0) {
   if (batch < 1 || total_q < 0 || total_kv < 0 || hq < 1) return false;
   // sum_b ceil(L_b / 128) <= total / 128 + batch when sum_b L_b <= total
   const long long cq = static_cast<long long>(total_q) / teattn::kBlockM + batch + 1;
@@ -95,6 +96,8 @@ bool make_layout(int batch, int total_q, int total_kv, int hq, bool backward, La
   off += static_cast<size_t>(cq) * hq * teattn::kBlockM * dq_cols * sizeof(float);
   L->dq_sem = off;
   if (dq_cols > 0) off = align_up(off + static_cast<size_t>(cq) * hq * sizeof(int), 256);
+  L->k_items = off;
+  if (dq_cols > 0) off = align_up(off + static_cast<size_t>(ck) * hkv * 4 * sizeof(int), 256);
   L->total = off;
   return true;
 }
@@ -237,9 +240,8 @@ size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
 }
 
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
-  (void)hkv;
   Layout L;
-  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_cols(d)) ? L.total : 0;
+  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_cols(d), hkv) ? L.total : 0;
 }
 
 size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
@@ -439,7 +441,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
   Layout L;
   const int cols = fused_cols(d);
   bool fused = false;
-  if (cols > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, cols) &&
+  if (cols > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, cols, hkv) &&
       workspace_bytes >= L.total) {
     fused = true;
   } else {
@@ -476,6 +478,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
     p.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
     p.dq_sem = reinterpret_cast<int*>(ws + L.dq_sem);
     p.dq_cols = cols;
+    p.k_items = reinterpret_cast<int4*>(ws + L.k_items);
   }
   int* pref_q = reinterpret_cast<int*>(ws + L.pref_q);
   p.pref_q = pref_q;

@@ -193,13 +193,15 @@ def test_selftest_and_status_reads_check_arguments(lib):
 def test_backward_workspace_sizes(lib):
     """For head dims up to 128 the default backward workspace adds the fused path's
     dQ accumulator (one 128-row fp32 tile of 64 or 128 columns per query tile and
-    head) and a counter per tile to the minimum one; for d = 256 the two agree."""
+    head), a counter per tile and its work-item list to the minimum one; for d = 256
+    the two agree."""
     B, T, hq, hkv = 7, 32960, 32, 8
     cap_q = T // 128 + B + 1
     for d, cols in ((128, 128), (96, 128), (64, 64), (8, 64)):
         full = lib.te_attn_bwd_workspace_size(B, T, T, hq, hkv, d)
         small = lib.te_attn_bwd_workspace_size_min(B, T, T, hq, hkv, d)
-        extra = cap_q * hq * 128 * cols * 4 + cap_q * hq * 4
+        cap_k = T // 128 + B + 1
+        extra = cap_q * hq * 128 * cols * 4 + cap_q * hq * 4 + cap_k * hkv * 16
         assert extra <= full - small <= extra + 512, (d, full - small, extra)
     assert (lib.te_attn_bwd_workspace_size(B, T, T, hq, hkv, 256)
             == lib.te_attn_bwd_workspace_size_min(B, T, T, hq, hkv, 256))
