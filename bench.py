@@ -346,19 +346,21 @@ def measure_variants(ta, w, t, flops, fwd_flops, flush, dev, steps=20, warmup=5)
     ms = time_calls(sbhd_step, flush, steps, warmup)
     out["sbhd_fwd_bwd"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
                            "shape": f"[{S}, {B}, h, d] with the workload's real lengths"}
-    # A/B of the backward: the two-kernel path (separate dQ kernel recomputing S and
-    # dP), selected by a workspace of the minimum size, against the default.
+    # A/B of the backward: the default two-kernel path (separate dQ kernel recomputing
+    # S and dP) against the fused one (one pass, ordered fp32 dQ accumulation).
     Tq, hq, d = t["q"].shape
     Tk, hkv, _ = t["k"].shape
     o = torch.empty_like(t["q"])
     l = torch.empty((Tq, hq), dtype=torch.float32, device=dev)
     ta.fwd(t["q"], t["k"], t["v"], *cu, w.attn_scale, w.mask_type, out=o, lse=l)
     g = [torch.empty_like(t[n]) for n in ("q", "k", "v")]
-    for name, size in (("bwd_default", ta.bwd_workspace_size(w.batch, Tq, Tk, hq, hkv, d)),
-                       ("bwd_two_kernel", ta.bwd_workspace_size_min(w.batch, Tq, Tk, hq, hkv, d))):
+    for name, fused in (("bwd_default", False), ("bwd_fused", True)):
+        size = (ta.bwd_fused_workspace_size if fused else ta.bwd_workspace_size)(
+            w.batch, Tq, Tk, hq, hkv, d)
         ws = torch.empty(size, dtype=torch.uint8, device=dev)
         ms = time_calls(lambda: ta.bwd(t["q"], t["k"], t["v"], o, t["dout"], l, *cu, w.attn_scale,
-                                       w.mask_type, dq=g[0], dk=g[1], dv=g[2], workspace=ws),
+                                       w.mask_type, dq=g[0], dk=g[1], dv=g[2], workspace=ws,
+                                       fused=fused),
                         flush, steps, warmup)
         out[name] = {"ms": ms, "tflops": 2.5 * fwd_flops / (ms * 1e-3) / 1e12,
                      "workspace_bytes": size}

@@ -32,7 +32,7 @@ from ._binding import (  # noqa: F401
     profile_enable,
     profile_read,
     bwd_workspace_size,
-    bwd_workspace_size_min,
+    bwd_fused_workspace_size,
     library,
     library_path,
     read_status,

@@ -70,7 +70,7 @@ def library(debug: bool = None) -> ctypes.CDLL:
     L.te_attn_version.restype = i32
     L.te_attn_version.argtypes = []
     for name in ("te_attn_fwd_workspace_size", "te_attn_bwd_workspace_size",
-                 "te_attn_bwd_workspace_size_min"):
+                 "te_attn_bwd_fused_workspace_size"):
         fn = getattr(L, name)
         fn.restype = sz
         fn.argtypes = [i32] * 6
@@ -78,6 +78,8 @@ def library(debug: bool = None) -> ctypes.CDLL:
     L.te_attn_fwd_thd.argtypes = [vp] * 5 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_bwd_thd.restype = i32
     L.te_attn_bwd_thd.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
+    L.te_attn_bwd_thd_fused.restype = i32
+    L.te_attn_bwd_thd_fused.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp]
     L.te_attn_bwd_thd_ev.restype = i32
     L.te_attn_bwd_thd_ev.argtypes = [vp] * 9 + [vp] * 4 + [i32] * 8 + [f32, i32, i32, vp, sz, vp, vp]
     L.te_attn_bwd_thd_noalloc.restype = i32
@@ -155,13 +157,12 @@ def fwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
 
 
 def bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
-    """Workspace bytes of the backward's fastest path (the fused one for d <= 128)."""
     return int(library().te_attn_bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d))
 
 
-def bwd_workspace_size_min(batch, total_q, total_kv, hq, hkv, d) -> int:
-    """Smallest workspace the backward accepts (it then runs the two-kernel path)."""
-    return int(library().te_attn_bwd_workspace_size_min(batch, total_q, total_kv, hq, hkv, d))
+def bwd_fused_workspace_size(batch, total_q, total_kv, hq, hkv, d) -> int:
+    """Workspace bytes of ``te_attn_bwd_thd_fused`` (0 for head dims above 128)."""
+    return int(library().te_attn_bwd_fused_workspace_size(batch, total_q, total_kv, hq, hkv, d))
 
 
 def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
@@ -199,10 +200,11 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv
 def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
         cu_seqlens_kv_padded, attn_scale, mask_type="padding", max_seqlen_q=0,
         max_seqlen_kv=0, dq=None, dk=None, dv=None, workspace=None, stream=None,
-        dq_done=None):
+        dq_done=None, fused=False):
     """``te_attn_bwd_thd``: returns ``(dq, dk, dv)`` in q's dtype. With ``dq_done``
     (a ``torch.cuda.Event``) it calls ``te_attn_bwd_thd_ev`` instead, which records
-    that event on the stream as soon as dq is final (before dk/dv are computed)."""
+    that event on the stream as soon as dq is final (before dk/dv are computed).
+    ``fused=True`` calls ``te_attn_bwd_thd_fused`` (head dims up to 128)."""
     L = library()
     _need_cuda(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                cu_seqlens_kv_padded, dq, dk, dv, workspace)
@@ -217,7 +219,9 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = bwd_workspace_size(B, Tq, Tk, hq, hkv, d)
+    if fused and dq_done is not None:
+        raise ValueError("the fused backward records no dq hand-over event")
+    need = (bwd_fused_workspace_size if fused else bwd_workspace_size)(B, Tq, Tk, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
@@ -227,7 +231,9 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padde
             d, float(attn_scale), _mask(mask_type), _DTYPES[q.dtype], _ptr(workspace),
             workspace.numel(), ctypes.c_void_p(st))
     with _on(q):
-        if dq_done is None:
+        if fused:
+            rc = L.te_attn_bwd_thd_fused(*args)
+        elif dq_done is None:
             rc = L.te_attn_bwd_thd(*args)
         else:
             if dq_done.cuda_event == 0:  # torch creates the CUDA event on its first record

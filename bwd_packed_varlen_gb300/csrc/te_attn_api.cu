@@ -2,10 +2,9 @@
 // workspace layout and the launch sequence of each call.
 //
 //   forward : schedule -> attention forward -> zero fill of rows no tile writes
-//   backward: schedule -> zero fill -> D = rowsum(dO * O) -> then either
-//             fused dK/dV/dQ -> dQ conversion           (head_dim <= 128, full workspace)
-//             dQ -> dK/dV                               (head_dim 256, or a workspace of
-//                                                        te_attn_bwd_workspace_size_min)
+//   backward: schedule -> zero fill -> D = rowsum(dO * O) -> dQ -> dK/dV
+//   fused backward (te_attn_bwd_thd_fused, head_dim <= 128): schedule -> zero fill
+//             -> D -> dK/dV with an ordered dQ accumulation -> dQ conversion
 //
 // All launches go to the caller's stream; nothing is allocated and nothing is
 // kept between calls except per-device constants (SM count).
@@ -240,15 +239,17 @@ size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, 
 }
 
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
-  Layout L;
-  return make_layout(batch, total_q, total_kv, hq, true, &L, fused_cols(d), hkv) ? L.total : 0;
-}
-
-size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv, int d) {
   (void)hkv;
   (void)d;
   Layout L;
   return make_layout(batch, total_q, total_kv, hq, true, &L) ? L.total : 0;
+}
+
+size_t te_attn_bwd_fused_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                        int d) {
+  Layout L;
+  const int cols = fused_cols(d);
+  return cols > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, cols, hkv) ? L.total : 0;
 }
 
 // Per-tensor dequantisation factors of an e4m3 forward (real value = stored
@@ -430,27 +431,21 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* out
                     const int32_t* cu_seqlens_kv_padded, int batch, int total_q, int total_kv,
                     int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
                     void* workspace, size_t workspace_bytes, void* stream, cudaEvent_t dq_done,
-                    bool sbhd) {
+                    bool sbhd, bool fused = false) {
   int rc = teattn::bwd_check_args(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv,
                                   cu_seqlens_q_padded, cu_seqlens_kv_padded, batch, total_q,
                                   total_kv, hq, hkv, d, attn_scale, mask_type, dtype);
   if (rc != TE_OK) return rc;
   if (!workspace) return fail(TE_ERR_INVALID_ARG, "workspace must not be NULL");
-  // The fused backward needs the dQ accumulator; a workspace of only the minimum
-  // size (or head_dim 256) takes the separate dQ kernel instead.
+  const int cols = fused ? fused_cols(d) : 0;
+  if (fused && cols == 0) return fail(TE_ERR_UNSUPPORTED, "the fused backward needs head dim <= 128");
   Layout L;
-  const int cols = fused_cols(d);
-  bool fused = false;
-  if (cols > 0 && make_layout(batch, total_q, total_kv, hq, true, &L, cols, hkv) &&
-      workspace_bytes >= L.total) {
-    fused = true;
-  } else {
-    if (!make_layout(batch, total_q, total_kv, hq, true, &L))
-      return fail(TE_ERR_INVALID_ARG, "sizes out of range");
-    if (workspace_bytes < L.total)
-      return fail(TE_ERR_WORKSPACE_TOO_SMALL,
-                  "workspace smaller than te_attn_bwd_workspace_size_min()");
-  }
+  if (!make_layout(batch, total_q, total_kv, hq, true, &L, cols, hkv))
+    return fail(TE_ERR_INVALID_ARG, "sizes out of range");
+  if (workspace_bytes < L.total)
+    return fail(TE_ERR_WORKSPACE_TOO_SMALL,
+                fused ? "workspace smaller than te_attn_bwd_fused_workspace_size()"
+                      : "workspace smaller than te_attn_bwd_workspace_size()");
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return fail(TE_ERR_CUDA, "no CUDA device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -533,6 +528,20 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
   return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
                   cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
                   dtype, workspace, workspace_bytes, stream, nullptr, false);
+}
+
+int te_attn_bwd_thd_fused(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                          int batch, int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv,
+                          int hq, int hkv, int d, float attn_scale, int mask_type, int dtype,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_kv;
+  return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                  cu_seqlens_kv_padded, batch, total_q, total_kv, hq, hkv, d, attn_scale, mask_type,
+                  dtype, workspace, workspace_bytes, stream, nullptr, false, true);
 }
 
 int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out, const void* dout,

@@ -129,9 +129,7 @@ int te_attn_bwd_thd_noalloc(const void* q, const void* k, const void* v, const v
                                         batch, total_q, total_kv, hq, hkv, d, attn_scale,
                                         mask_type, dtype);
   if (rc != TE_OK) return rc;
-  // te_attn_bwd_thd then runs the fused path if its workspace fits, else the
-  // two-kernel path, whose smaller workspace must fit
-  const size_t need = te_attn_bwd_workspace_size_min(batch, total_q, total_kv, hq, hkv, d);
+  const size_t need = te_attn_bwd_workspace_size(batch, total_q, total_kv, hq, hkv, d);
   if (need > kNoAllocScratchBytes) {
     teattn::set_last_error("problem needs " + std::to_string(need) +
                            " bytes of scratch, more than the built-in " +

@@ -121,20 +121,9 @@ int te_attn_version(void);
 size_t te_attn_fwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
                                   int d);
 
-/*
- * Bytes of workspace te_attn_bwd_thd needs for these sizes (0 on invalid sizes):
- * with it, head dims up to 128 run the fused backward, whose dQ accumulator
- * (fp32, one 128-row tile of 64 or 128 columns per query tile and head) is part of
- * the workspace. te_attn_bwd_workspace_size_min() is the smallest workspace the
- * backward accepts: with less than te_attn_bwd_workspace_size() bytes (and for
- * d > 128 always) it runs the two-kernel path, a separate dQ kernel that
- * recomputes the scores. Both paths are deterministic and meet the same tolerances;
- * they are not bit-identical to each other (dQ is summed in a different order).
- */
+/* Bytes of workspace te_attn_bwd_thd needs for these sizes (0 on invalid sizes). */
 size_t te_attn_bwd_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
                                   int d);
-size_t te_attn_bwd_workspace_size_min(int batch, int total_q, int total_kv, int hq, int hkv,
-                                      int d);
 
 /*
  * Forward: writes out [total_q, hq, d] and lse [total_q, hq] (natural-log softmax
@@ -154,11 +143,9 @@ int te_attn_fwd_thd(const void* q, const void* k, const void* v, void* out, floa
  * dk and dv [total_kv, hkv, d]. dk/dv of a key/value head sum over the hq/hkv query
  * heads of its group inside one thread block (no atomics). The arguments mirror
  * TransformerEngine's fused_attn_bwd as [2448] calls it (out and lse are
- * inputs; dropout 0; no bias; deterministic).
- * Fused path (d <= 128, workspace of te_attn_bwd_workspace_size()): one kernel
- * computes dK, dV and each key tile's share of dQ; the shares of a (query tile,
- * head) are added into the fp32 accumulator in a fixed order (descending key
- * tiles, ordered by a counter per tile), so dq is bit-identical from call to call.
+ * inputs; dropout 0; no bias; deterministic). dq comes from a separate kernel that
+ * owns each query tile and recomputes its scores, so no partial sums of dq ever
+ * meet in global memory.
  */
 int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -172,10 +159,9 @@ int te_attn_bwd_thd(const void* q, const void* k, const void* v, const void* out
 /*
  * Backward with a hand-over point (no counterpart in the pages): identical results
  * to te_attn_bwd_thd, plus `dq_done`, a cudaEvent_t created by the caller (or NULL),
- * is recorded on `stream` as soon as dq is final -- on the two-kernel path the
- * backward computes dq before dk and dv, so that the caller can start consuming dq
- * (a copy to the host, a collective) on another stream while dk/dv are still being
- * computed; on the fused path dq, dk and dv become final together. Returns what
+ * is recorded on `stream` as soon as dq is final -- the backward computes dq before
+ * dk and dv -- so that the caller can start consuming dq (a copy to the host, a
+ * collective) on another stream while dk/dv are still being computed. Returns what
  * te_attn_bwd_thd returns, or TE_ERR_CUDA if the event cannot be recorded.
  */
 int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* out,
@@ -186,6 +172,34 @@ int te_attn_bwd_thd_ev(const void* q, const void* k, const void* v, const void* 
                        int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
                        int mask_type, int dtype, void* workspace, size_t workspace_bytes,
                        void* stream, void* dq_done);
+
+/*
+ * Fused backward (no counterpart in the pages' code; the deterministic fused dQ of
+ * the FlashAttention line of backward kernels, done without atomics in any varying
+ * order): the same arguments and results, within the same tolerances, as
+ * te_attn_bwd_thd, for head dims up to 128 (TE_ERR_UNSUPPORTED above). One kernel
+ * computes dK, dV and each key tile's share of dQ from a single pass over the
+ * scores -- five products instead of seven -- and adds the shares of every
+ * (query tile, head) into an fp32 accumulator in the workspace in a fixed order
+ * (descending key tiles, ordered by a counter per tile); a conversion kernel then
+ * writes dq. Repeated calls are bit-identical; the results are not bit-identical to
+ * te_attn_bwd_thd's (dq is summed in another order). The workspace, of
+ * te_attn_bwd_fused_workspace_size() bytes, holds the accumulator (4 bytes per
+ * padded query row, head and column, the head dim rounded up to 64 or 128).
+ * On GB300 this path is slower than te_attn_bwd_thd at the sizes measured here:
+ * moving each key tile's 64 KB fp32 share out of the SM costs more than the two
+ * recomputed products save.
+ */
+size_t te_attn_bwd_fused_workspace_size(int batch, int total_q, int total_kv, int hq, int hkv,
+                                        int d);
+int te_attn_bwd_thd_fused(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded,
+                          int batch, int total_q, int total_kv, int max_seqlen_q,
+                          int max_seqlen_kv, int hq, int hkv, int d, float attn_scale,
+                          int mask_type, int dtype, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /*
  * Sequence-major layout ("sbhd", the layout of [3216]'s reproduction: q, k, v of
@@ -310,10 +324,8 @@ int te_attn_profile_read(double* total_ms, int* launches);
  *   or events).
  * - Arguments are checked first, with the codes and messages of te_attn_bwd_thd;
  *   then TE_ERR_WORKSPACE_TOO_SMALL (and a message naming the size needed) is
- *   returned when te_attn_bwd_workspace_size_min() of the problem exceeds the array.
- *   Otherwise the results are those of te_attn_bwd_thd given a workspace of the
- *   array's size, bit for bit: the fused path when te_attn_bwd_workspace_size() of
- *   the problem fits in the array, the two-kernel path otherwise.
+ *   returned when te_attn_bwd_workspace_size() of the problem exceeds the array.
+ *   Otherwise the results are those of te_attn_bwd_thd, bit for bit.
  * - Device-side errors (TE_STATUS_* bits) land in the array's status word:
  *   te_attn_read_status_noalloc() reads them for the current device.
  */

@@ -191,17 +191,25 @@ def test_selftest_and_status_reads_check_arguments(lib):
 
 
 def test_backward_workspace_sizes(lib):
-    """For head dims up to 128 the default backward workspace adds the fused path's
-    dQ accumulator (one 128-row fp32 tile of 64 or 128 columns per query tile and
-    head), a counter per tile and its work-item list to the minimum one; for d = 256
-    the two agree."""
+    """The fused backward's workspace adds its dQ accumulator (one 128-row fp32 tile
+    of 64 or 128 columns per query tile and head), a counter per tile and its
+    work-item list to the two-kernel backward's; it has none for d = 256."""
     B, T, hq, hkv = 7, 32960, 32, 8
     cap_q = T // 128 + B + 1
+    cap_k = T // 128 + B + 1
     for d, cols in ((128, 128), (96, 128), (64, 64), (8, 64)):
-        full = lib.te_attn_bwd_workspace_size(B, T, T, hq, hkv, d)
-        small = lib.te_attn_bwd_workspace_size_min(B, T, T, hq, hkv, d)
-        cap_k = T // 128 + B + 1
+        full = lib.te_attn_bwd_fused_workspace_size(B, T, T, hq, hkv, d)
+        small = lib.te_attn_bwd_workspace_size(B, T, T, hq, hkv, d)
         extra = cap_q * hq * 128 * cols * 4 + cap_q * hq * 4 + cap_k * hkv * 16
         assert extra <= full - small <= extra + 512, (d, full - small, extra)
-    assert (lib.te_attn_bwd_workspace_size(B, T, T, hq, hkv, 256)
-            == lib.te_attn_bwd_workspace_size_min(B, T, T, hq, hkv, 256))
+    assert lib.te_attn_bwd_fused_workspace_size(B, T, T, hq, hkv, 256) == 0
+    P = ctypes.c_void_p(1 << 20)
+    cu = ctypes.c_void_p(1 << 21)
+    big = ctypes.c_size_t(1 << 40)
+    # head dim above 128: unsupported, before any launch
+    assert lib.te_attn_bwd_thd_fused(P, P, P, P, P, P, P, P, P, cu, cu, cu, cu, 2, 64, 64, 0, 0, 4,
+                                     2, 256, 0.1, 1, 1, P, big, None) == -2
+    # the two-kernel backward's workspace is too small for the fused one
+    small = lib.te_attn_bwd_workspace_size(2, 64, 64, 4, 2, 128)
+    assert lib.te_attn_bwd_thd_fused(P, P, P, P, P, P, P, P, P, cu, cu, cu, cu, 2, 64, 64, 0, 0, 4,
+                                     2, 128, 0.1, 1, 1, P, ctypes.c_size_t(small), None) == -3

@@ -1,5 +1,5 @@
-"""The fused backward (dK, dV and an ordered dQ in one kernel, head_dim <= 128)
-against the oracle, and the two-kernel path it replaces by default.
+"""The fused backward te_attn_bwd_thd_fused (dK, dV and an ordered dQ in one kernel,
+head_dim <= 128) against the oracle, beside the default two-kernel backward.
 
 Deterministic results are the requirement of [2448] ("Expected behavior": dk/dv
 must not depend on earlier calls; TransformerEngine's deterministic flag): the fused
@@ -26,15 +26,16 @@ def _bits(x):
     return x.view(torch.int32 if x.dtype == torch.float32 else torch.int16)
 
 
-def _ws(w, minimal, fill=None):
+def _ws(w, fused=True):
     import bwd_packed_varlen_gb300 as ta
     Tq, hq, d = w.q.shape
     Tk, hkv, _ = w.k.shape
-    f = ta.bwd_workspace_size_min if minimal else ta.bwd_workspace_size
-    ws = torch.empty(f(w.batch, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device="cuda")
-    if fill is not None:
-        ws.fill_(fill)
-    return ws
+    f = ta.bwd_fused_workspace_size if fused else ta.bwd_workspace_size
+    return torch.empty(f(w.batch, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device="cuda")
+
+
+def _fused(ws):
+    return {"workspace": ws, "fused": True}
 
 
 CASES = [
@@ -54,10 +55,10 @@ def test_both_backward_paths_match_oracle(case):
     import bwd_packed_varlen_gb300 as ta
     w = W.random_varlen(*case)
     t = to_dev(w)
-    fused = gpu_fwd_bwd(w, t, bwd={"workspace": _ws(w, False)})
-    two = gpu_fwd_bwd(w, t, bwd={"workspace": _ws(w, True)})
-    assert ta.bwd_workspace_size(w.batch, *w.q.shape[:1], w.k.shape[0], w.hq, w.hkv, w.d) > \
-        ta.bwd_workspace_size_min(w.batch, *w.q.shape[:1], w.k.shape[0], w.hq, w.hkv, w.d)
+    ws = _ws(w)
+    fused = gpu_fwd_bwd(w, t, bwd=_fused(ws))
+    assert ta.read_status(ws) == 0
+    two = gpu_fwd_bwd(w, t, bwd={"workspace": _ws(w, False)})
     check_against_oracle(w, fused)
     check_against_oracle(w, two)
 
@@ -70,13 +71,13 @@ def test_fused_bitwise_across_order_and_poison():
     wa = W.random_varlen(86, 6, 900, 8, 2, 128, W.MASK_PADDING_CAUSAL, "bf16")
     wb = W.random_varlen(87, 3, 1200, 8, 2, 128, W.MASK_PADDING, "bf16")
     ta_, tb_ = to_dev(wa), to_dev(wb)
-    size = max(_ws(wa, False).numel(), _ws(wb, False).numel())
+    size = max(_ws(wa).numel(), _ws(wb).numel())
     ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
     first = {}
     for order in ("ABA", "BAB"):
         for name in order:
             w, t = (wa, ta_) if name == "A" else (wb, tb_)
-            res = gpu_fwd_bwd(w, t, bwd={"workspace": ws})
+            res = gpu_fwd_bwd(w, t, bwd=_fused(ws))
             assert ta.read_status(ws) == 0
             if name not in first:
                 first[name] = res
@@ -84,7 +85,7 @@ def test_fused_bitwise_across_order_and_poison():
                 for a, b in zip(first[name], res):
                     assert torch.equal(_bits(a), _bits(b))
     ws.fill_(0xFF)
-    res = gpu_fwd_bwd(wa, ta_, bwd={"workspace": ws})
+    res = gpu_fwd_bwd(wa, ta_, bwd=_fused(ws))
     assert ta.read_status(ws) == 0
     for a, b in zip(first["A"], res):
         assert torch.equal(_bits(a), _bits(b))
@@ -111,10 +112,21 @@ def test_fused_long_chains_finish(mask):
                    cu_seqlens_kv_padded=cu(pads), attn_scale=1.0 / math.sqrt(128),
                    mask_type=mask, dtype="bf16")
     t = to_dev(w)
-    ws = _ws(w, False)
-    res = gpu_fwd_bwd(w, t, bwd={"workspace": ws})
+    ws = _ws(w)
+    res = gpu_fwd_bwd(w, t, bwd=_fused(ws))
     assert ta.read_status(ws) == 0
     check_against_oracle(w, res)
-    again = gpu_fwd_bwd(w, t, bwd={"workspace": ws})
+    again = gpu_fwd_bwd(w, t, bwd=_fused(ws))
     for a, b in zip(res, again):
         assert torch.equal(_bits(a), _bits(b))
+
+
+def test_fused_rejects_head_dim_256():
+    import bwd_packed_varlen_gb300 as ta
+    w = W.random_varlen(89, 2, 200, 2, 1, 256, W.MASK_PADDING, "bf16")
+    t = to_dev(w)
+    assert ta.bwd_fused_workspace_size(w.batch, w.q.shape[0], w.k.shape[0], 2, 1, 256) == 0
+    with pytest.raises(ta.TeAttnError) as e:
+        gpu_fwd_bwd(w, t, bwd={"workspace": torch.empty(1 << 20, dtype=torch.uint8, device="cuda"),
+                               "fused": True})
+    assert e.value.code == -2
