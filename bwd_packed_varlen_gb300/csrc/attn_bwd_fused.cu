@@ -36,16 +36,19 @@
 // The same order puts each dependency G steps ahead: key tile kt + 1 reaches query
 // tile qt one query tile (G steps) earlier in its sweep than key tile kt does.
 //
-// Roles (640 threads): 16 compute warps (warp w owns TMEM lanes 32*(w%4).. and
-// query columns [32*(w/4), +32) of S^T and dP^T, output columns [kD/4*(w/4), +kD/4)
-// of dK, dV and dQ); a TMA producer warp; an MMA warp (lane 0 issues every
-// tcgen05.mma); two reducer warps (lane 0) that add the staged dQ tiles of even and
-// odd steps to the accumulator with bulk reductions, so the compute warps never
-// wait on global memory. The compute warps stage dQ_t in the step's Q and dO
-// buffers (columns [0, kD/2) and [kD/2, kD) in fp32), which are free once dQ_t is
-// done: their last readers, dK_t and dV_t, ran before it. The producer refills the
-// stage once the reducer has read the staged tile, so a reducer has a whole step
-// to take its tile.
+// Roles (768 threads, six warpgroups): 16 compute warps (warp w owns TMEM lanes
+// 32*(w%4).. and query columns [32*(w/4), +32) of S^T and dP^T, output columns
+// [kD/4*(w/4), +kD/4) of dK and dV); a TMA producer warp; an MMA warp (lane 0 issues
+// every tcgen05.mma); two reducer warps (lane 0) that add the staged dQ tiles of
+// even and odd steps to the accumulator with bulk reductions; and four drain warps
+// (one per TMEM lane quarter) that read dQ_t out of TMEM and stage it, so neither
+// the compute warps nor the MMA warp ever wait on dQ's way to global memory. dQ_t
+// is staged in the step's Q and dO buffers (columns [0, kD/2) and [kD/2, kD) in
+// fp32), which are free once dQ_t is done: their last readers, dK_t and dV_t, ran
+// before it. The producer refills the stage once the reducer has read the staged
+// tile, so a reducer has a whole step to take its tile. Registers: launched at 80
+// a thread, the compute warpgroups take 96 and the others give up to 48
+// (512 * 96 + 256 * 48 = 768 * 80).
 // A block claims its next item only once it has issued the loads of its current
 // item's last step, so items start about in the order they are claimed and the key
 // tile a block waits on is normally already ahead of it.
@@ -77,7 +80,12 @@ using fused_elem_t = typename std::conditional<kBF16, __nv_bfloat16, __half>::ty
 constexpr int kFusedComputeWarps = 16;
 constexpr int kFusedComputeThreads = kFusedComputeWarps * 32;
 constexpr int kFusedWarpProducer = 16, kFusedWarpMma = 17, kFusedWarpReducer = 18;
-constexpr int kFusedThreads = 20 * 32;
+constexpr int kFusedWarpDrain = 20, kFusedDrainThreads = 4 * 32;
+constexpr int kFusedThreads = 24 * 32;
+// per-thread registers after the split (launch: 65536 / 768 rounded down to 80)
+constexpr int kFusedRegsCompute = 96, kFusedRegsOther = 48;
+static_assert(16 * 32 * kFusedRegsCompute + 8 * 32 * kFusedRegsOther == kFusedThreads * 80,
+              "register split must equal the launch allocation");
 
 // Barriers and the work ring live at the end of dynamic shared memory (the kernel
 // has no static shared memory, so the dynamic base keeps its 1024-byte alignment).
@@ -163,15 +171,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.q_full[i], 1);
       mbar_init(&B.q_empty[i], 1);
-      mbar_init(&B.stage_full[i], kFusedComputeWarps);
+      mbar_init(&B.stage_full[i], 4);
     }
     mbar_init(&B.s_full, 1);
     mbar_init(&B.dp_full, 1);
     mbar_init(&B.p_ready, kFusedComputeThreads);
     mbar_init(&B.ds_ready, kFusedComputeThreads);
     mbar_init(&B.dq_full, 1);
-    mbar_init(&B.y_free, kFusedComputeThreads);
-    ring_init(B.ring, 1 + kFusedComputeThreads + 2);
+    mbar_init(&B.y_free, kFusedDrainThreads);
+    ring_init(B.ring, 1 + kFusedComputeThreads + 2 + kFusedDrainThreads);
     fence_barrier_init();
   }
   if (warp == kFusedWarpMma) {
@@ -200,6 +208,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     return it;
   };
 
+  if (warp >= kFusedComputeWarps) {
+  // Warpgroups 4 and 5 (producer, MMA, reducers, drain) give registers back; each
+  // warpgroup executes the same setmaxnreg before splitting into its roles.
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kFusedRegsOther));
   if (warp == kFusedWarpProducer) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
@@ -337,6 +349,48 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         mma_commit(&B.acc_full);
       }
     }
+  } else if (warp >= kFusedWarpDrain) {
+    // ------------------------------------------------------------- drain
+    // dQ_t out of Y in 16-column chunks into the fp32 staging of the step (Q buffer:
+    // columns [0, kD/2), dO buffer: the rest; [128 rows][kD/2] per half, 16-byte
+    // unit u of a row at (u ^ row % 8): the accumulator's layout). Y is handed back
+    // after the last chunk has been read, before its stores.
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int row_in_tile = quarter * 32 + lane;
+    const int sw = row_in_tile & 7;
+    int it = 0, ii = 0;
+    bool ok = true;
+    for (; ok; ++ii) {
+      const int item = ring_get_warp(B.ring, ii, status, &ok);
+      if (!ok || item < 0) break;
+      const Item I = decode(item);
+      for (int t = 0; t < I.steps; ++t, ++it) {
+        const int st = it & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&B.dq_full, it & 1, status));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tmem + S::kColY + lane_base + c * 16, o);
+          tmem_ld_wait();
+          if (c == kD / 16 - 1) {
+            tc_fence_before();
+            mbar_arrive(&B.y_free);
+          }
+          const int col = c * 16;  // first column of the chunk
+          uint8_t* row = (col < kD / 2 ? sQ : sDO) + st * S::kTileBytes + row_in_tile * S::kHalfRowBytes;
+          const int u0 = (col % (kD / 2)) / 4;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(row + (((u0 + v) ^ sw) << 4), o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.stage_full[it & 1]);
+      }
+    }
   } else if (warp >= kFusedWarpReducer) {
     // ------------------------------------------------------------- reducers
     // Reducer r adds the dQ tiles of the steps with (step & 1) == r.
@@ -387,7 +441,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
       }
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFusedRegsCompute));
     // ------------------------------------------------------------- compute
     const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -484,7 +540,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         tmem_st16(tmem + S::kColX + lane_base + col0 + 16, dd);
         {
-          // dS tile (its last reader, dQ of the previous step, is done): row = key,
+          // dS tile (its last reader, dQ_t-1, finished before dP^T_t, which this
+          // phase waited for): row = key,
           // 16-byte unit u of queries [8u, 8u+8) in 64-query chunks, 128-byte
           // swizzled (unit ^ row % 8) -- dQ's A operand, MN-major (queries contiguous).
           uint8_t* row = sDS + (grp >> 1) * 16384 + row_in_tile * 128;
@@ -498,30 +555,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B.ds_ready);
-        // ---- C: drain dQ_t from Y, stage it for the reducer
-        ok = __all_sync(0xffffffffu, mbar_wait(&B.dq_full, it & 1, status));
-        if (!ok) break;
-        tc_fence_after();
-        {
-          uint32_t o[S::kOutCols];
-          if constexpr (S::kOutCols == 32) tmem_ld32(tmem + S::kColY + lane_base + grp * 32, o);
-          else tmem_ld16(tmem + S::kColY + lane_base + grp * 16, *reinterpret_cast<uint32_t(*)[16]>(o));
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&B.y_free);
-          // fp32 staging, [128 rows][kD/2 columns] per half (Q buffer: columns
-          // [0, kD/2), dO buffer: the rest), 16-byte unit u of a row stored at
-          // (u ^ row % 8): the accumulator's layout.
-          uint8_t* half = (grp < 2 ? sQ : sDO) + st * S::kTileBytes;
-          uint8_t* row = half + row_in_tile * S::kHalfRowBytes;
-          const int u0 = (grp & 1) * (S::kOutCols / 4);
-#pragma unroll
-          for (int v = 0; v < S::kOutCols / 4; ++v)
-            st_shared_v4(row + (((u0 + v) ^ sw) << 4), o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.stage_full[it & 1]);
       }
       if (!ok) break;
       // Epilogue: scale * dK and dV for key rows some real query sees.
