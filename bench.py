@@ -171,25 +171,31 @@ def gpu_uuid(dev):
         return None
 
 
-def kernel_source_hash():
+# Sources each kernel's code comes from (its file and the headers it includes).
+_HEADERS = ["common.cuh", "sm103_ptx.cuh", "row_store.cuh", "work_queue.cuh", "tmap.h"]
+KERNEL_SOURCES = {"fwd": ["attn_fwd_pair.cu"] + _HEADERS, "dkdv": ["attn_bwd.cu"] + _HEADERS,
+                  "dq": ["attn_bwd.cu"] + _HEADERS, "bwd_fused": ["attn_bwd_fused.cu"] + _HEADERS}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bwd_packed_varlen_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+    """Per-launch DRAM bytes of `kernel` from the committed ncu record, if it was
+    taken on the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     try:
-        t = json.load(open(path))
-        if t.get("source_hash") != kernel_source_hash():
+        k = json.load(open(path)).get("kernels", {}).get(kernel, {})
+        if k.get("source_hash") != kernel_source_hash(kernel):
             return None
-        return t.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch_full")
+        return k.get("dram_bytes_per_launch_full")
     except Exception:
         return None
 

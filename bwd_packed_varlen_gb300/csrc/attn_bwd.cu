@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* status = p.header + kHdrStatus;
   const int per_pair = p.hkv * S::kSplit;
-  const int n_items = p.header[kHdrNumKPairs] * per_pair;
+  const int n_pairs = p.header[kHdrNumKPairs];
+  const int n_items = n_pairs * per_pair;
   const bool causal = p.causal != 0;
 
   if (tid == 0) {
@@ -162,10 +163,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
   auto decode = [&](int item) {
     Item it;
-    const int2 pr = p.k_pairs[item / per_pair];
-    const int rem = item % per_pair;
-    it.g = rem / S::kSplit;
-    it.split = rem % S::kSplit;
+    const PairHead ph = item_pair_head(item, n_pairs, S::kSplit);
+    const int2 pr = p.k_pairs[ph.pair];
+    it.g = ph.head / S::kSplit;
+    it.split = ph.head % S::kSplit;
     it.kt = pr.y;
     it.b = pr.x;
     it.s = load_seq(p, pr.x);
@@ -514,7 +515,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* status = p.header + kHdrStatus;
-  const int n_items = p.header[kHdrNumQPairs] * p.hq;
+  const int n_pairs = p.header[kHdrNumQPairs];
+  const int n_items = n_pairs * p.hq;
   const bool causal = p.causal != 0;
 
   if (tid == 0) {
@@ -562,8 +564,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int n = 0;
         // Query tiles that see no key (rows before a lower-right causal triangle)
         // are left to the zero fill and never reach the ring.
+        PairHead ph{0, 0};
         while (item >= 0) {
-          pr = p.q_pairs[item / p.hq];
+          ph = item_pair_head(item, n_pairs, p.group);
+          pr = p.q_pairs[ph.pair];
           s = load_seq(p, pr.x);
           n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
           if (n > 0) break;
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = ring_put(ring, ii, -1, status);
           break;
         }
-        const int h = item % p.hq, g = h / p.group;
+        const int h = ph.head, g = h / p.group;
         // the step count travels with the item: the MMA thread then needs no global loads
         if (!(ok = ring_put(ring, ii, item, status, n))) break;
         nxt = next_item(p.header + kHdrNextDq);  // used at the next hand-over
@@ -691,8 +695,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto decode = [&](int item) {
       RowItem r{item, 0, 0, false, 0, 0.f, 0.f};
       if (item < 0) return r;
-      const int2 pr = p.q_pairs[item / p.hq];
-      const int h = item % p.hq;
+      const PairHead ph = item_pair_head(item, n_pairs, p.group);
+      const int2 pr = p.q_pairs[ph.pair];
+      const int h = ph.head;
       const SeqInfo s = load_seq(p, pr.x);
       r.n = (visible_keys(s, pr.y, causal) + kBN - 1) / kBN;
       const int row = pr.y * kBlockM + quarter * 32 + lane;

@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(192, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* status = p.header + kHdrStatus;
-  const int n_items = p.header[kHdrNumQPairs] * p.hq;
+  const int n_pairs = p.header[kHdrNumQPairs];
+  const int n_items = n_pairs * p.hq;
   const bool causal = p.causal != 0;
 
   if (tid == 0) {
@@ -112,8 +113,9 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0, ii = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int2 pr = p.q_pairs[item / p.hq];
-        const int h = item % p.hq, g = h / p.group;
+        const PairHead ph = item_pair_head(item, n_pairs, p.group);
+        const int2 pr = p.q_pairs[ph.pair];
+        const int h = ph.head, g = h / p.group;
         const SeqInfo s = load_seq(p, pr.x);
         const int qt = pr.y;
         const int n = (visible_keys(s, qt, causal) + kBlockN - 1) / kBlockN;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(192, 1)
         return true;
       };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int2 pr = p.q_pairs[item / p.hq];
+        const int2 pr = p.q_pairs[item_pair_head(item, n_pairs, p.group).pair];
         const SeqInfo s = load_seq(p, pr.x);
         const int n = (visible_keys(s, pr.y, causal) + kBlockN - 1) / kBlockN;
         if (n == 0) continue;
@@ -206,8 +208,9 @@ __global__ void __launch_bounds__(192, 1)
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int2 pr = p.q_pairs[item / p.hq];
-      const int h = item % p.hq;
+      const PairHead ph = item_pair_head(item, n_pairs, p.group);
+      const int2 pr = p.q_pairs[ph.pair];
+      const int h = ph.head;
       const SeqInfo s = load_seq(p, pr.x);
       const int qt = pr.y;
       const int n = (visible_keys(s, qt, causal) + kBlockN - 1) / kBlockN;

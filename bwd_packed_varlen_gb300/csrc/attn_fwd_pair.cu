@@ -70,8 +70,9 @@ struct FwdItem {
 
 __device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool causal) {
   FwdItem I;
-  const int2 pr = p.f_pairs[item / p.hq];
-  I.h = item % p.hq;
+  const PairHead ph = item_pair_head(item, p.header[kHdrNumFPairs], p.group);
+  const int2 pr = p.f_pairs[ph.pair];
+  I.h = ph.head;
   I.g = I.h / p.group;
   I.u = pr.y;
   I.s = load_seq(p, pr.x);

@@ -195,6 +195,21 @@ __device__ __forceinline__ int row_keys(const SeqInfo& s, int i, bool causal) {
   return causal ? min(s.len_k, max(0, i + 1 + s.diag)) : s.len_k;
 }
 
+// Work items of the per-head kernels are numbered group-major: all items of kv
+// head group 0, then group 1, ...; within a group the pairs in list order (longest
+// first) with the group's heads innermost. Blocks running at the same time then
+// work on one group's heads, whose Q/dO and K/V tiles stay in L2, rather than on
+// every head of a sequence at once. `heads_per_group`: query heads per kv head for
+// the per-query-head kernels, the column splits of one kv head for dK/dV.
+struct PairHead {
+  int pair, head;
+};
+__device__ __forceinline__ PairHead item_pair_head(int item, int n_pairs, int heads_per_group) {
+  const int per_group = n_pairs * heads_per_group;
+  const int g = item / per_group, r = item - g * per_group;
+  return PairHead{r / heads_per_group, g * heads_per_group + r % heads_per_group};
+}
+
 // Number of key rows a query tile can see (the keys its last real row sees).
 __device__ __forceinline__ int visible_keys(const SeqInfo& s, int q_tile, bool causal) {
   if (!causal) return s.len_k;
