@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["throughput", "small"], default="throughput",
                     help="small: the same recipe with 8192 real tokens (for ncu captures)")
+    ap.add_argument("--bwd", choices=["two-kernel", "fused"], default="two-kernel",
+                    help="backward of the timed step: te_attn_bwd_thd (dQ and dK/dV kernels) "
+                         "or te_attn_bwd_thd_fused (one pass)")
     ap.add_argument("--configs", action="store_true",
                     help="time every configuration beside the CPU oracle (one line each)")
     return ap.parse_args()
@@ -426,7 +429,9 @@ def run_ours(args, rank, world, local_rank):
     lse = torch.empty((Tq, hq), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
     wsf = torch.empty(ta.fwd_workspace_size(B, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(ta.bwd_workspace_size(B, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device=dev)
+    fused = args.bwd == "fused"
+    wsb = torch.empty((ta.bwd_fused_workspace_size if fused else ta.bwd_workspace_size)(
+        B, Tq, Tk, hq, hkv, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     cu = (t["cu_seqlens_q"], t["cu_seqlens_kv"], t["cu_seqlens_q_padded"], t["cu_seqlens_kv_padded"])
 
@@ -434,7 +439,7 @@ def run_ours(args, rank, world, local_rank):
         ta.fwd(q, k, v, *cus, w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv,
                out=out, lse=lse, workspace=wsf)
         ta.bwd(q, k, v, out, do, lse, *cus, w.attn_scale, w.mask_type, w.max_seqlen_q,
-               w.max_seqlen_kv, dq=dq, dk=dk, dv=dv, workspace=wsb)
+               w.max_seqlen_kv, dq=dq, dk=dk, dv=dv, workspace=wsb, fused=fused)
 
     def barrier():
         if world > 1:
@@ -538,7 +543,9 @@ def run_ours(args, rank, world, local_rank):
             ev_dq = ev()
             ta.bwd(buf["q"], buf["k"], buf["v"], out, buf["dout"], lse, *cus_d,
                    w.attn_scale, w.mask_type, w.max_seqlen_q, w.max_seqlen_kv, dq=dq, dk=dk, dv=dv,
-                   workspace=wsb, dq_done=ev_dq)
+                   workspace=wsb, dq_done=None if fused else ev_dq, fused=fused)
+            if fused:
+                ev_dq.record(main)
             ev_bwd = ev()
             ev_bwd.record(main)
             in_free[i % 2] = ev_bwd
@@ -629,7 +636,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": dict(workload_config(w), backward=(
+            "te_attn_bwd_thd_fused" if fused else "te_attn_bwd_thd (dQ, dK/dV kernels)")),
         "pct_peak": {"burst": value / world / peaks["bf16_tflops"],
                      "sustained": value / world / peaks["bf16_tflops_sustained"],
                      "source": peaks["source"]},
