@@ -280,7 +280,6 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + S::col_s(x) + lane_base;
     const uint32_t t_o = tmem + S::col_o(x) + lane_base;
-    const float sl2 = p.scale_log2;
     using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
     int ns = 0, no = 0;  // S hand-overs and items seen by this tile
     bool ok = true;
@@ -321,42 +320,74 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         tc_fence_after();
         const int nvalid = min(max(lim - j * kBlockN, 0), kBlockN);
         const bool full = __all_sync(0xffffffffu, nvalid >= kBlockN);
-        // pass 1: row max over the four 32-column chunks (4 independent 3-input chains)
-        float mp[4];
+        const float sl2 = p.scale_log2;
+        // A row's first tile with a visible key: its max, to start the offset m.
+        if (__any_sync(0xffffffffu, m == -INFINITY && nvalid > 0)) {
+          float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mp[k] = -INFINITY;
+          for (int k = 0; k < kBlockN / 32; ++k) {
+            uint32_t sv[32];
+            tmem_ld32(t_s + 32 * k, sv);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-          uint32_t sv[32];
-          tmem_ld32(t_s + c0, sv);
-          tmem_ld_wait();
-          if (full) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              mp[(c >> 1) & 3] = max3(mp[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              mp[(c >> 1) & 3] = max3(mp[(c >> 1) & 3], c0 + c < nvalid ? __uint_as_float(sv[c]) : -INFINITY,
-                                      c0 + c + 1 < nvalid ? __uint_as_float(sv[c + 1]) : -INFINITY);
+            for (int c = 0; c < 16; ++c)
+              mp[c & 3] = max3(mp[c & 3], 32 * k + 2 * c < nvalid ? __uint_as_float(sv[2 * c]) : -INFINITY,
+                               32 * k + 2 * c + 1 < nvalid ? __uint_as_float(sv[2 * c + 1]) : -INFINITY);
           }
+          if (m == -INFINITY && nvalid > 0) m = fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]) * sl2;
         }
-        const float mx = fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]);
-        const float mxs = mx * sl2;
-        float m_new = m;
-        bool rescale = false;
-        if (nvalid > 0) {
-          if (m == -INFINITY) {
-            m_new = mxs;
-          } else if (mxs > m + 8.0f) {
-            m_new = mxs;
-            rescale = true;
-          }
-        }
+        // One pass over S: P = exp2(S * scale*log2e - m), its row sum and the row max
+        // together, P held in registers until the pass is accepted. The offset is
+        // raised lazily: only when a row's max exceeds m + 8 does that row take the
+        // new max, O and l are scaled by exp2(m_old - m_new) (O is final for the
+        // tiles before this one: S(j) was issued after P V(j-1)) and the pass is
+        // repeated; S is still intact in TMEM then, as P is written only at the end.
         float alpha = 1.f;
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O_x is final for tiles < j: S_x(j) was issued after PV_x(j-1).
-          alpha = rescale ? ex2f(m - m_new) : 1.f;
+        uint64_t sp[4];
+        uint32_t pk[kBlockN / 32][16];
+        // the pass, as straight-line code for full tiles and for masked ones
+        auto pass = [&](auto full_tag) -> float {
+          constexpr bool kFull = decltype(full_tag)::value;
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m, -m);
+          float mp[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            sp[k] = f2_pack(0.f, 0.f);
+            mp[k] = -INFINITY;
+          }
+#pragma unroll
+          for (int k = 0; k < kBlockN / 32; ++k) {
+            uint32_t sv[32];
+            tmem_ld32(t_s + 32 * k, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float s0 = __uint_as_float(sv[2 * c]), s1 = __uint_as_float(sv[2 * c + 1]);
+              const float2 xx = f2_unpack(ffma2(f2_pack(s0, s1), sl2x2, negm2));
+              float p0 = ex2f(xx.x), p1 = ex2f(xx.y);
+              if constexpr (!kFull) {
+                const bool v0 = 32 * k + 2 * c < nvalid, v1 = 32 * k + 2 * c + 1 < nvalid;
+                p0 = v0 ? p0 : 0.f;
+                p1 = v1 ? p1 : 0.f;
+                s0 = v0 ? s0 : -INFINITY;
+                s1 = v1 ? s1 : -INFINITY;
+              }
+              mp[c & 3] = max3(mp[c & 3], s0, s1);
+              sp[c & 3] = fadd2(sp[c & 3], f2_pack(p0, p1));
+              pk[k][c] = pack2<kBF16>(p0, p1);
+            }
+          }
+          return fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]) * sl2;
+        };
+        for (;;) {
+          const float mxs = full ? pass(std::true_type{}) : pass(std::false_type{});
+          const bool raise = nvalid > 0 && mxs > m + 8.0f;
+          if (!__any_sync(0xffffffffu, raise)) break;
+          // rare: a row's max grew by more than 2^8
+          if (raise) {
+            alpha = ex2f(m - mxs);
+            m = mxs;
+          }
 #pragma unroll
           for (int c0 = 0; c0 < kD; c0 += 32) {
             uint32_t o[32];
@@ -368,39 +399,14 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
             tmem_st16(t_o + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
           }
         }
-        // pass 2: P = exp2(S * scale * log2e - m), packed over the chunk's first
-        // half-width columns (chunk c writes [16c, 16c+16), already read)
-        // x = s * scale*log2e - m on pairs; sums accumulate in 4 paired partials
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_new, -m_new);
-        uint64_t sp[4];
+        // P (16-bit) over the first half of the S columns
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sp[k] = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-          uint32_t sv[32], pk[16];
-          tmem_ld32(t_s + c0, sv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float2 xx = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])),
-                                              sl2x2, negm2));
-            float p0 = ex2f(xx.x), p1 = ex2f(xx.y);
-            if (!full) {
-              p0 = c0 + 2 * c < nvalid ? p0 : 0.f;
-              p1 = c0 + 2 * c + 1 < nvalid ? p1 : 0.f;
-            }
-            sp[c & 3] = fadd2(sp[c & 3], f2_pack(p0, p1));
-            pk[c] = pack2<kBF16>(p0, p1);
-          }
-          tmem_st16(t_s + c0 / 2, pk);
-        }
+        for (int k = 0; k < kBlockN / 32; ++k) tmem_st16(t_s + 16 * k, pk[k]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar_p_ready[x]);
         const float2 s01 = f2_unpack(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
-        const float rs = s01.x + s01.y;
-        l = l * alpha + rs;
-        m = m_new;
+        l = l * alpha + (s01.x + s01.y);
       }
       if (!ok) break;
       const RowItem nxt = decode(ring_get_warp(ring, ii + 1, status, &ok));
