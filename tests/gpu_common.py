@@ -105,7 +105,7 @@ def row_elem_check(got, ref, ms, u):
 
 
 def assert_close(name, got, ref, ms, u):
-    """Whole tensor (the benchmark spec's rel. Frobenius and cosine), then every element and
+    """Whole tensor (relative Frobenius error and cosine), then every element and
     every row against the bounds above; ms = (m1, m2) magnitude sums of this tensor."""
     rel, cos = rel_cos(got, ref)
     assert rel <= REL_TOL and cos >= COS_TOL, f"{name}: rel={rel:.3e} cos={cos:.6f}"
