@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
   auto decode = [&](int item) {
     Item it;
-    const PairHead ph = item_pair_head(item, n_pairs, S::kSplit);
+    const PairHead ph = item_pair_head_banded(item, n_pairs, per_pair);
     const int2 pr = p.k_pairs[ph.pair];
     it.g = ph.head / S::kSplit;
     it.split = ph.head % S::kSplit;

@@ -210,6 +210,23 @@ __device__ __forceinline__ PairHead item_pair_head(int item, int n_pairs, int he
   return PairHead{r / heads_per_group, g * heads_per_group + r % heads_per_group};
 }
 
+// dK/dV items: the sorted key-tile list is cut into bands of kBand consecutive
+// pairs, and within a band the items go head-major (all of the band's pairs for
+// head 0, then head 1, ...). Whole-list group-major order would start the last
+// groups' longest key tiles late and leave SMs idle at the end of the kernel; the
+// bands keep the list's longest-first order at band granularity while items of
+// one kv head still run side by side. `heads`: kv heads x column splits.
+__device__ __forceinline__ PairHead item_pair_head_banded(int item, int n_pairs, int heads) {
+  constexpr int kBand = 64;
+  const int full = n_pairs / kBand, in_full = full * kBand * heads;
+  if (item < in_full) {
+    const int c = item / (kBand * heads), r = item - c * (kBand * heads);
+    return PairHead{c * kBand + r % kBand, r / kBand};
+  }
+  const int last = n_pairs - full * kBand, r = item - in_full;
+  return PairHead{full * kBand + r % last, r / last};
+}
+
 // Number of key rows a query tile can see (the keys its last real row sees).
 __device__ __forceinline__ int visible_keys(const SeqInfo& s, int q_tile, bool causal) {
   if (!causal) return s.len_k;
