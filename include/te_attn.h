@@ -61,6 +61,12 @@
  * Streams: every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *   default stream); no host synchronisation. Calls that share a workspace must be
  *   ordered (same stream or explicit events).
+ * CUDA graphs: the compute entry points neither allocate nor synchronise, so a
+ *   sequence of calls can be captured into a graph and replayed; each replay reads
+ *   the buffers' contents at replay time and gives the bits an eager call would.
+ *   Make one eager call of each entry point before capturing (the first call sets
+ *   kernel attributes). Not capturable: te_attn_read_status*, te_attn_profile_read
+ *   (they synchronise) and profiling itself.
  *
  * Errors: functions return TE_OK (0) or a negative TE_ERR_* code, and
  *   te_attn_last_error() gives a thread-local message. Host-detectable argument
