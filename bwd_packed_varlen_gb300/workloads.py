@@ -247,6 +247,39 @@ def throughput(seed: int = 5, tensor_seed: int = 55, hq: int = 32, hkv: int = 8,
         meta={"lengths": lengths, "padded": padded})
 
 
+def growing_scores(seed: int = 11, lengths=(700, 513, 300), hq: int = 4, hkv: int = 2,
+                   d: int = 64, mask_type: int = MASK_PADDING_CAUSAL, dtype: str = "bf16",
+                   growth: float = 1.5):
+    """Scores that rise along the key axis for every other query row: key j gets
+    growth * (j / 128) times a fixed direction u (|u|^2 = d) added to its N(0,1)
+    entries, odd query rows get u added. With scale 1/sqrt(d), an odd row's score
+    against key j then carries growth * sqrt(d) * j / 128, i.e. it grows by
+    growth * sqrt(d) per 128 keys (12 for the defaults, over 17 in log2 units): a
+    running row maximum moves by more than 2^8 from one key tile to the next, while
+    even rows stay nearly flat. Packed, padded by 0-5 rows per sequence."""
+    rng = np.random.default_rng(seed)
+    lens = list(lengths)
+    pads = [x + int(rng.integers(0, 6)) for x in lens]
+    T = int(sum(pads))
+    u = rng.standard_normal(d).astype(np.float32)
+    u *= np.float32(math.sqrt(d) / np.linalg.norm(u))
+    q = _normal(rng, (T, hq, d))
+    k = _normal(rng, (T, hkv, d))
+    v = _normal(rng, (T, hkv, d))
+    do = _normal(rng, (T, hq, d))
+    off = 0
+    for L, P in zip(lens, pads):
+        j = np.arange(P, dtype=np.float32)
+        k[off:off + P] += (growth * j / 128.0)[:, None, None] * u[None, None, :]
+        q[off + 1:off + P:2] += u[None, None, :]
+        off += P
+    return Workload(
+        name=f"growing_scores_{seed}", q=_to(q, dtype), k=_to(k, dtype), v=_to(v, dtype),
+        dout=_to(do, dtype), cu_seqlens_q=_cu(lens), cu_seqlens_kv=_cu(lens),
+        cu_seqlens_q_padded=_cu(pads), cu_seqlens_kv_padded=_cu(pads),
+        attn_scale=1.0 / math.sqrt(d), mask_type=mask_type, dtype=dtype)
+
+
 def random_varlen(seed: int, batch: int, max_len: int, hq: int, hkv: int, d: int,
                   mask_type: int, dtype: str = "bf16", pad_max: int = 17,
                   allow_empty: bool = True, tail: int = 5, kv_differs: bool = True):

@@ -18,6 +18,7 @@ from bwd_packed_varlen_gb300 import workloads as W
 from gpu_common import (
     UNIT_ROUNDOFF,
     assert_close,
+    row_elem_check,
     check_against_oracle,
     error_scales,
     gpu_fwd_bwd,
@@ -189,6 +190,49 @@ def test_bottom_right_causal(d):
     for x, y in zip(br, tl):
         assert _same_bits(x, y)
 
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mask", [W.MASK_PADDING_CAUSAL, W.MASK_PADDING])
+def test_running_max_raised_between_key_tiles(d, dtype, mask):
+    """Odd query rows whose scores climb by more than 2^8 per key tile, even rows
+    flat: the forward raises the running max (scaling O and l, and redoing the
+    tile's exponentials) on most tiles for half the rows of every warp. The forward
+    is held to the oracle. The backward is held to the interface's definition from
+    the oracle's out (rounded to the storage dtype) and lse, element by element and
+    row by row. A raise means later keys outweigh earlier ones by more than 2^8, so
+    these rows are peaked: dS = P (dP - D) cancels, and rounding dS to bf16 before
+    dS K -- which any tensor-core backward does -- moves dQ by 1-2 % of its norm
+    (the arithmetic, emulated in float64 on the CPU, gives the same). The
+    whole-tensor 1e-2 bar is therefore applied to dQ only in fp16."""
+    import bwd_packed_varlen_gb300 as ta
+    w = W.growing_scores(d=d, dtype=dtype, mask_type=mask)
+    t = to_dev(w)
+    cu = (t["cu_q"], t["cu_kv"], t["cu_q_pad"], t["cu_kv_pad"])
+    out, lse = ta.fwd(t["q"], t["k"], t["v"], *cu, w.attn_scale, w.mask_type)
+    r_out, r_lse, _, _, _ = oracle_fwd_bwd(w)
+    scales = error_scales(w)
+    u = UNIT_ROUNDOFF[w.dtype]
+    assert_close("out", np64(out), r_out, scales[0], u)
+    got_lse, fin = np64(lse), np.isfinite(r_lse)
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(r_lse))
+    assert np.abs(got_lse[fin] - r_lse[fin]).max() <= 1e-3
+
+    o16 = torch.from_numpy(r_out).to(w.q.dtype)
+    l32 = torch.from_numpy(r_lse).to(torch.float32)
+    ref = oracle.attn_bwd_thd(np64(w.q), np64(w.k), np64(w.v), np64(o16), np64(w.dout),
+                              l32.double().numpy(), w.cu_seqlens_q.numpy(),
+                              w.cu_seqlens_kv.numpy(), w.cu_seqlens_q_padded.numpy(),
+                              w.cu_seqlens_kv_padded.numpy(), w.attn_scale, w.mask_type)
+    dq, dk, dv = ta.bwd(t["q"], t["k"], t["v"], o16.cuda(), t["dout"], l32.cuda(), *cu,
+                        w.attn_scale, w.mask_type)
+    for nm, a, b, m in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, scales[1:]):
+        if nm == "dq" and dtype == "bf16":
+            c = row_elem_check(np64(a), b, m, u)
+            assert c["elem_ratio"] <= 1.0 and c["row_ratio"] <= 1.0, c
+        else:
+            assert_close(nm, np64(a), b, m, u)
 
 def test_all_sequences_empty_and_keyless():
     """A batch where every query sequence is empty, and one where queries exist but
