@@ -234,6 +234,23 @@ def test_running_max_raised_between_key_tiles(d, dtype, mask):
         else:
             assert_close(nm, np64(a), b, m, u)
 
+
+@pytest.mark.parametrize("lengths", [[1024] * 8, [1024] * 8 + [100], [1024] * 16 + [129, 1]],
+                         ids=["64_key_tiles", "65_key_tiles", "131_key_tiles"])
+def test_key_tile_list_band_boundaries(lengths):
+    """dK/dV items come in bands of 64 sorted key tiles (kv-head-major inside a
+    band): exactly one full band, one full band plus one tile, and two full bands
+    plus three tiles must each cover every (key tile, kv head) once."""
+    rng = np.random.default_rng(len(lengths))
+    T, hq, hkv, d = sum(lengths), 4, 2, 32
+    q, k, v, do = (torch.from_numpy(rng.standard_normal((T, h, d), dtype=np.float32)).to(torch.bfloat16)
+                   for h in (hq, hkv, hkv, hq))
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    w = W.Workload(name="bands", q=q, k=k, v=v, dout=do, cu_seqlens_q=cu, cu_seqlens_kv=cu,
+                   cu_seqlens_q_padded=cu.clone(), cu_seqlens_kv_padded=cu.clone(),
+                   attn_scale=d ** -0.5, mask_type=W.MASK_PADDING_CAUSAL, dtype="bf16")
+    check_against_oracle(w, gpu_fwd_bwd(w))
+
 def test_all_sequences_empty_and_keyless():
     """A batch where every query sequence is empty, and one where queries exist but
     no keys: outputs are exact zeros (lse -inf on real keyless queries)."""
