@@ -115,3 +115,41 @@ def test_debug_build_d256_and_sbhd():
         assert ta.read_status(ws) == 0
     for a, b in zip((out, lse) + tuple(ref), (out_d, lse_d) + tuple(got)):
         assert torch.equal(_bits(a), _bits(b))
+
+
+def test_debug_build_fused_backward_and_e4m3_forward():
+    """The opt-in paths under the bounds checks -- the fused backward (ordered fp32
+    dQ accumulation, then the conversion kernel) and the e4m3 forward (V widened in
+    the workspace) -- and the default backward on a packing whose key tiles fill
+    more than one 64-tile band of the dK/dV item order; each bit-identical to the
+    release build."""
+    import bwd_packed_varlen_gb300 as ta
+    w = W.random_varlen(74, 14, 1200, 4, 2, 128, W.MASK_PADDING_CAUSAL, "bf16")  # 106 key tiles
+    t = to_dev(w)
+    Tq, hq, d = w.q.shape
+    Tk, hkv, _ = w.k.shape
+    cu = (t["cu_q"], t["cu_kv"], t["cu_q_pad"], t["cu_kv_pad"])
+    out, lse = ta.fwd(t["q"], t["k"], t["v"], *cu, w.attn_scale, w.mask_type)
+    release = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, w.attn_scale,
+                     w.mask_type, fused=True)
+    two_kernel = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, w.attn_scale,
+                        w.mask_type)
+    f8 = torch.float8_e4m3fn
+    q8, k8, v8 = (x.to(f8) for x in (t["q"], t["k"], t["v"]))
+    rel_e4 = ta.fwd_e4m3(q8, k8, v8, *cu, w.attn_scale, 1.0, 1.0, 1.0, w.mask_type)
+    wsb = torch.empty(ta.bwd_fused_workspace_size(w.batch, Tq, Tk, hq, hkv, d),
+                      dtype=torch.uint8, device="cuda")
+    with ta.debug_build():
+        debug = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, w.attn_scale,
+                       w.mask_type, workspace=wsb, fused=True)
+        assert ta.read_status(wsb) == 0
+        dbg_e4 = ta.fwd_e4m3(q8, k8, v8, *cu, w.attn_scale, 1.0, 1.0, 1.0, w.mask_type)
+        ws2 = torch.empty(ta.bwd_workspace_size(w.batch, Tq, Tk, hq, hkv, d),
+                          dtype=torch.uint8, device="cuda")
+        dbg_two = ta.bwd(t["q"], t["k"], t["v"], out, t["dout"], lse, *cu, w.attn_scale,
+                         w.mask_type, workspace=ws2)
+        assert ta.read_status(ws2) == 0
+    torch.cuda.synchronize()
+    for a, b in zip(tuple(release) + tuple(rel_e4) + tuple(two_kernel),
+                    tuple(debug) + tuple(dbg_e4) + tuple(dbg_two)):
+        assert torch.equal(_bits(a), _bits(b))
