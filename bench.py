@@ -601,6 +601,8 @@ def run_ours(args, rank, world, local_rank):
         if name in credited:
             ent["tflops_credited"] = credited[name] / (avg * 1e-3) / 1e12
             ent["tflops_executed"] = executed[name] / (avg * 1e-3) / 1e12
+            ent["frac_credited"] = ent["tflops_credited"] / peaks["bf16_tflops"]
+            ent["frac_executed"] = ent["tflops_executed"] / peaks["bf16_tflops"]
         kernels[name] = ent
     dom = max(("fwd", "dkdv", "dq", "bwd_fused"),
               key=lambda n: kernels.get(n, {}).get("total_ms", 0.0))
