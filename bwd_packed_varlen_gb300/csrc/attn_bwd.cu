@@ -350,13 +350,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           else tmem_ld16(tmem + S::kColST + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(sv));
           tmem_ld_wait();
           if (full) {
+            // paired fma: one instruction for two entries, same rounding as fmaf
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
             for (int k = 0; k < kG / 4; ++k) {
               const float4 l4 = lse4[k];
-              pv[4 * k] = ex2b(fmaf(__uint_as_float(sv[4 * k]), sl2, -l4.x));
-              pv[4 * k + 1] = ex2b(fmaf(__uint_as_float(sv[4 * k + 1]), sl2, -l4.y));
-              pv[4 * k + 2] = ex2b(fmaf(__uint_as_float(sv[4 * k + 2]), sl2, -l4.z));
-              pv[4 * k + 3] = ex2b(fmaf(__uint_as_float(sv[4 * k + 3]), sl2, -l4.w));
+              const float2 x01 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])),
+                                                 sl2x2, f2_pack(-l4.x, -l4.y)));
+              const float2 x23 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])),
+                                                 sl2x2, f2_pack(-l4.z, -l4.w)));
+              pv[4 * k] = ex2b(x01.x);
+              pv[4 * k + 1] = ex2b(x01.y);
+              pv[4 * k + 2] = ex2b(x23.x);
+              pv[4 * k + 3] = ex2b(x23.y);
             }
           } else {
 #pragma unroll
@@ -392,13 +398,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // Masked entries are selected to 0 (not multiplied): D of rows past the
           // query length is never written and may hold any bits.
           float r[kG];
+          // paired subtract and multiply: the same two roundings per entry
 #pragma unroll
           for (int k = 0; k < kG / 4; ++k) {
             const float4 d4 = dlt4[k];
-            r[4 * k] = pv[4 * k] * (__uint_as_float(dv[4 * k]) - d4.x);
-            r[4 * k + 1] = pv[4 * k + 1] * (__uint_as_float(dv[4 * k + 1]) - d4.y);
-            r[4 * k + 2] = pv[4 * k + 2] * (__uint_as_float(dv[4 * k + 2]) - d4.z);
-            r[4 * k + 3] = pv[4 * k + 3] * (__uint_as_float(dv[4 * k + 3]) - d4.w);
+            const float2 r01 = f2_unpack(fmul2(f2_pack(pv[4 * k], pv[4 * k + 1]),
+                                               fadd2(f2_pack(__uint_as_float(dv[4 * k]), __uint_as_float(dv[4 * k + 1])),
+                                                     f2_pack(-d4.x, -d4.y))));
+            const float2 r23 = f2_unpack(fmul2(f2_pack(pv[4 * k + 2], pv[4 * k + 3]),
+                                               fadd2(f2_pack(__uint_as_float(dv[4 * k + 2]), __uint_as_float(dv[4 * k + 3])),
+                                                     f2_pack(-d4.z, -d4.w))));
+            r[4 * k] = r01.x;
+            r[4 * k + 1] = r01.y;
+            r[4 * k + 2] = r23.x;
+            r[4 * k + 3] = r23.y;
           }
           if (!full) {
 #pragma unroll
@@ -738,8 +751,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar_s_free);
           if (__all_sync(0xffffffffu, nvalid >= kG)) {
+            // paired fma: one instruction for two entries, same rounding as fmaf
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-            for (int i = 0; i < kG; ++i) pv[i] = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
+            for (int i = 0; i < kG; i += 2) {
+              const float2 xx = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                                                sl2x2, nl2));
+              pv[i] = ex2b(xx.x);
+              pv[i + 1] = ex2b(xx.y);
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < kG; ++i) {
@@ -764,11 +784,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if constexpr (kG == 32) tmem_ld32(tmem + S::kColDP + lane_base + col0, dv);
           else tmem_ld16(tmem + S::kColDP + lane_base + col0, *reinterpret_cast<uint32_t(*)[16]>(dv));
           tmem_ld_wait();
+          // paired subtract and multiply: the same two roundings per entry
           uint32_t dd[kG / 2];
+          const uint64_t nd2 = f2_pack(-dlt, -dlt);
 #pragma unroll
-          for (int k = 0; k < kG / 2; ++k)
-            dd[k] = pack2<kBF16>(pv[2 * k] * (__uint_as_float(dv[2 * k]) - dlt),
-                                 pv[2 * k + 1] * (__uint_as_float(dv[2 * k + 1]) - dlt));
+          for (int k = 0; k < kG / 2; ++k) {
+            const float2 r = f2_unpack(fmul2(f2_pack(pv[2 * k], pv[2 * k + 1]),
+                                             fadd2(f2_pack(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])), nd2)));
+            dd[k] = pack2<kBF16>(r.x, r.y);
+          }
           const uint32_t ds_col = S::kColDS + (it & 1) * S::kDsCols + grp * (kG / 2);
           if constexpr (kG == 32) tmem_st16(tmem + ds_col + lane_base, dd);
           else tmem_st8(tmem + ds_col + lane_base, *reinterpret_cast<uint32_t(*)[8]>(dd));
