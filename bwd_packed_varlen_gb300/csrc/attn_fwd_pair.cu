@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
         const int nvalid = min(max(lim - j * kBlockN, 0), kBlockN);
         const bool full = __all_sync(0xffffffffu, nvalid >= kBlockN);
         const float sl2 = p.scale_log2;
-        // A row's first tile with a visible key: its max, to start the offset m.
-        if (__any_sync(0xffffffffu, m == -INFINITY && nvalid > 0)) {
+        // Row max of this tile's visible scores (log2 domain), from S in TMEM.
+        auto tile_max = [&]() -> float {
           float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int k = 0; k < kBlockN / 32; ++k) {
@@ -334,27 +334,31 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
               mp[c & 3] = max3(mp[c & 3], 32 * k + 2 * c < nvalid ? __uint_as_float(sv[2 * c]) : -INFINITY,
                                32 * k + 2 * c + 1 < nvalid ? __uint_as_float(sv[2 * c + 1]) : -INFINITY);
           }
-          if (m == -INFINITY && nvalid > 0) m = fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]) * sl2;
+          return fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]) * sl2;
+        };
+        // A row's first tile with a visible key: its max, to start the offset m.
+        if (__any_sync(0xffffffffu, m == -INFINITY && nvalid > 0)) {
+          const float mxs = tile_max();
+          if (m == -INFINITY && nvalid > 0) m = mxs;
         }
-        // One pass over S: P = exp2(S * scale*log2e - m), its row sum and the row max
-        // together, P held in registers until the pass is accepted. The offset is
-        // raised lazily: only when a row's max exceeds m + 8 does that row take the
-        // new max, O and l are scaled by exp2(m_old - m_new) (O is final for the
-        // tiles before this one: S(j) was issued after P V(j-1)) and the pass is
-        // repeated; S is still intact in TMEM then, as P is written only at the end.
+        // One pass over S: P = exp2(S * scale*log2e - m) and its row sum, P held in
+        // registers until the pass is accepted. The offset is raised lazily: only
+        // when a row's max exceeds m + 8 does that row take the new max, O and l are
+        // scaled by exp2(m_old - m_new) (O is final for the tiles before this one:
+        // S(j) was issued after P V(j-1)) and the pass is repeated; S is still intact
+        // in TMEM then, as P is written only at the end. A row whose P sums to at
+        // most 2^8 has no entry above 2^8 and cannot need a raise, so the max itself
+        // is taken (in a second read of S) only for rows with a larger sum -- rare
+        // once a row's offset is set, and no max instructions in the common pass.
         float alpha = 1.f;
         uint64_t sp[4];
         uint32_t pk[kBlockN / 32][16];
         // the pass, as straight-line code for full tiles and for masked ones
-        auto pass = [&](auto full_tag) -> float {
+        auto pass = [&](auto full_tag) {
           constexpr bool kFull = decltype(full_tag)::value;
           const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m, -m);
-          float mp[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            sp[k] = f2_pack(0.f, 0.f);
-            mp[k] = -INFINITY;
-          }
+          for (int k = 0; k < 4; ++k) sp[k] = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < kBlockN / 32; ++k) {
             uint32_t sv[32];
@@ -362,25 +366,26 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              float s0 = __uint_as_float(sv[2 * c]), s1 = __uint_as_float(sv[2 * c + 1]);
-              const float2 xx = f2_unpack(ffma2(f2_pack(s0, s1), sl2x2, negm2));
+              const float2 xx = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])),
+                                                sl2x2, negm2));
               float p0 = ex2f(xx.x), p1 = ex2f(xx.y);
               if constexpr (!kFull) {
-                const bool v0 = 32 * k + 2 * c < nvalid, v1 = 32 * k + 2 * c + 1 < nvalid;
-                p0 = v0 ? p0 : 0.f;
-                p1 = v1 ? p1 : 0.f;
-                s0 = v0 ? s0 : -INFINITY;
-                s1 = v1 ? s1 : -INFINITY;
+                p0 = 32 * k + 2 * c < nvalid ? p0 : 0.f;
+                p1 = 32 * k + 2 * c + 1 < nvalid ? p1 : 0.f;
               }
-              mp[c & 3] = max3(mp[c & 3], s0, s1);
               sp[c & 3] = fadd2(sp[c & 3], f2_pack(p0, p1));
               pk[k][c] = pack2<kBF16>(p0, p1);
             }
           }
-          return fmaxf(max3(mp[0], mp[1], mp[2]), mp[3]) * sl2;
         };
         for (;;) {
-          const float mxs = full ? pass(std::true_type{}) : pass(std::false_type{});
+          if (full)
+            pass(std::true_type{});
+          else
+            pass(std::false_type{});
+          const float2 s01 = f2_unpack(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
+          if (!__any_sync(0xffffffffu, s01.x + s01.y > 256.0f)) break;
+          const float mxs = tile_max();
           const bool raise = nvalid > 0 && mxs > m + 8.0f;
           if (!__any_sync(0xffffffffu, raise)) break;
           // rare: a row's max grew by more than 2^8
