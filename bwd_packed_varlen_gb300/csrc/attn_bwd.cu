@@ -356,9 +356,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int k = 0; k < kG / 4; ++k) {
               const float4 l4 = lse4[k];
               const float2 x01 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])),
-                                                 sl2x2, f2_pack(-l4.x, -l4.y)));
+                                                 sl2x2, f2_pack(l4.x, l4.y)));
               const float2 x23 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])),
-                                                 sl2x2, f2_pack(-l4.z, -l4.w)));
+                                                 sl2x2, f2_pack(l4.z, l4.w)));
               pv[4 * k] = ex2b(x01.x);
               pv[4 * k + 1] = ex2b(x01.y);
               pv[4 * k + 2] = ex2b(x23.x);
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = 4 * k + e;
-                const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -l[e]));
+                const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, l[e]));
                 pv[i] = (i >= lo && i < hi) ? x : 0.f;
               }
             }
@@ -404,10 +404,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float4 d4 = dlt4[k];
             const float2 r01 = f2_unpack(fmul2(f2_pack(pv[4 * k], pv[4 * k + 1]),
                                                fadd2(f2_pack(__uint_as_float(dv[4 * k]), __uint_as_float(dv[4 * k + 1])),
-                                                     f2_pack(-d4.x, -d4.y))));
+                                                     f2_pack(d4.x, d4.y))));
             const float2 r23 = f2_unpack(fmul2(f2_pack(pv[4 * k + 2], pv[4 * k + 3]),
                                                fadd2(f2_pack(__uint_as_float(dv[4 * k + 2]), __uint_as_float(dv[4 * k + 3])),
-                                                     f2_pack(-d4.z, -d4.w))));
+                                                     f2_pack(d4.z, d4.w))));
             r[4 * k] = r01.x;
             r[4 * k + 1] = r01.y;
             r[4 * k + 2] = r23.x;
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int item, n, lim;
       bool row_valid;
       size_t gi;
-      float lse2, dlt;
+      float nlse2, ndlt;  // -lse * log2(e) and -D of this row
     };
     auto decode = [&](int item) {
       RowItem r{item, 0, 0, false, 0, 0.f, 0.f};
@@ -722,8 +722,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     bounds_ok(r.gi < static_cast<size_t>(p.total_q) * p.hq &&
                                   ti < static_cast<size_t>(p.pair_cap_q) * p.hq * kBlockM,
                               status);
-      r.lse2 = r.row_valid ? p.lse_t[ti] : 0.f;
-      r.dlt = r.row_valid ? p.delta_t[ti] : 0.f;
+      r.nlse2 = r.row_valid ? p.lse_t[ti] : 0.f;
+      r.ndlt = r.row_valid ? p.delta_t[ti] : 0.f;
       return r;
     };
     int it = 0, ii = 0;
@@ -731,10 +731,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));
     for (; ok && cur.item >= 0; ++ii) {
       const int n = cur.n, lim = cur.lim;
-      const float lse2 = cur.lse2, dlt = cur.dlt;
+      const float nlse2 = cur.nlse2, ndlt = cur.ndlt;
       for (int j = 0; j < n; ++j, ++it) {
         const int nvalid = lim - (j * kBN + col0);
-        // ---- phase A: P = exp2(S * scale * log2e - lse2) into registers, then free S
+        // ---- phase A: P = exp2(S * scale * log2e - nlse2) into registers, then free S
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, it & 1, status));
         if (!ok) break;
         tc_fence_after();
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive(&bar_s_free);
           if (__all_sync(0xffffffffu, nvalid >= kG)) {
             // paired fma: one instruction for two entries, same rounding as fmaf
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse2, nlse2);
 #pragma unroll
             for (int i = 0; i < kG; i += 2) {
               const float2 xx = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < kG; ++i) {
-              const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
+              const float x = ex2b(fmaf(__uint_as_float(sv[i]), sl2, nlse2));
               pv[i] = i < nvalid ? x : 0.f;
             }
           }
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
           // paired subtract and multiply: the same two roundings per entry
           uint32_t dd[kG / 2];
-          const uint64_t nd2 = f2_pack(-dlt, -dlt);
+          const uint64_t nd2 = f2_pack(ndlt, ndlt);
 #pragma unroll
           for (int k = 0; k < kG / 2; ++k) {
             const float2 r = f2_unpack(fmul2(f2_pack(pv[2 * k], pv[2 * k + 1]),

@@ -482,13 +482,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           tmem_ld32(tmem + S::kColX + lane_base + col0, sv);
           tmem_ld_wait();
           if (full) {
+            // paired fma (-lse * log2e arrives negated): same rounding as fmaf
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
             for (int k = 0; k < kG / 4; ++k) {
               const float4 l4 = lse4[k];
-              pv[4 * k] = ex2_fused(fmaf(__uint_as_float(sv[4 * k]), sl2, -l4.x));
-              pv[4 * k + 1] = ex2_fused(fmaf(__uint_as_float(sv[4 * k + 1]), sl2, -l4.y));
-              pv[4 * k + 2] = ex2_fused(fmaf(__uint_as_float(sv[4 * k + 2]), sl2, -l4.z));
-              pv[4 * k + 3] = ex2_fused(fmaf(__uint_as_float(sv[4 * k + 3]), sl2, -l4.w));
+              const float2 x01 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])),
+                                                 sl2x2, f2_pack(l4.x, l4.y)));
+              const float2 x23 = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])),
+                                                 sl2x2, f2_pack(l4.z, l4.w)));
+              pv[4 * k] = ex2_fused(x01.x);
+              pv[4 * k + 1] = ex2_fused(x01.y);
+              pv[4 * k + 2] = ex2_fused(x23.x);
+              pv[4 * k + 3] = ex2_fused(x23.y);
             }
           } else {
 #pragma unroll
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = 4 * k + e;
-                const float x = ex2_fused(fmaf(__uint_as_float(sv[i]), sl2, -l[e]));
+                const float x = ex2_fused(fmaf(__uint_as_float(sv[i]), sl2, l[e]));
                 pv[i] = (i >= lo && i < hi) ? x : 0.f;
               }
             }
@@ -523,13 +529,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           // Masked entries are selected to 0 (not multiplied): D of rows past the
           // query length is never written and may hold any bits.
           float rr[kG];
+          // paired add (-D arrives negated) and multiply: the same two roundings
 #pragma unroll
           for (int k = 0; k < kG / 4; ++k) {
             const float4 d4 = dlt4[k];
-            rr[4 * k] = pv[4 * k] * (__uint_as_float(dv[4 * k]) - d4.x);
-            rr[4 * k + 1] = pv[4 * k + 1] * (__uint_as_float(dv[4 * k + 1]) - d4.y);
-            rr[4 * k + 2] = pv[4 * k + 2] * (__uint_as_float(dv[4 * k + 2]) - d4.z);
-            rr[4 * k + 3] = pv[4 * k + 3] * (__uint_as_float(dv[4 * k + 3]) - d4.w);
+            const float2 r01 = f2_unpack(fmul2(f2_pack(pv[4 * k], pv[4 * k + 1]),
+                                               fadd2(f2_pack(__uint_as_float(dv[4 * k]), __uint_as_float(dv[4 * k + 1])),
+                                                     f2_pack(d4.x, d4.y))));
+            const float2 r23 = f2_unpack(fmul2(f2_pack(pv[4 * k + 2], pv[4 * k + 3]),
+                                               fadd2(f2_pack(__uint_as_float(dv[4 * k + 2]), __uint_as_float(dv[4 * k + 3])),
+                                                     f2_pack(d4.z, d4.w))));
+            rr[4 * k] = r01.x;
+            rr[4 * k + 1] = r01.y;
+            rr[4 * k + 2] = r23.x;
+            rr[4 * k + 3] = r23.y;
           }
           if (!full) {
 #pragma unroll

@@ -70,8 +70,8 @@ struct AttnParams {
   void* dv;
   // Backward, per (query tile pair, head) blocks of 128 rows in the natural pair
   // order (pair = pref_q[b] + row / 128): lse * log2(e) and D = rowsum(dO * O).
-  float* lse_t;
-  float* delta_t;
+  float* lse_t;    // -lse * log2(e), tile-major
+  float* delta_t;  // -D = -rowsum(dO * O), tile-major
   const int* pref_q;   // prefix sums of query tiles per sequence (scheduler output)
   // Fused backward: fp32 dQ accumulator, one 128-row tile of dq_cols (64 or 128)
   // columns per (natural query tile pair, head), and one int semaphore per (pair,

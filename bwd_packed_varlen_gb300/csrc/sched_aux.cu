@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
                    p.header + kHdrStatus))
       continue;
     for (int h = lane; h < p.hq; h += 32)
-      p.lse_t[t0 + static_cast<size_t>(h) * kBlockM] = p.lse_in[row * p.hq + h] * kLog2e;
+      p.lse_t[t0 + static_cast<size_t>(h) * kBlockM] = -(p.lse_in[row * p.hq + h] * kLog2e);
     const uint4* o = reinterpret_cast<const uint4*>(static_cast<const T*>(p.out_in) +
                                                     row * p.hq * p.d);
     const uint4* g = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) +
@@ -416,14 +416,14 @@ __global__ void __launch_bounds__(256) delta_kernel(AttnParams p) {
           float v = c < chunks ? dot8<T>(oa[u], ga[u]) : 0.f;
           for (int w = cpr >> 1; w > 0; w >>= 1) v += __shfl_xor_sync(0xffffffffu, v, w);
           if (c < chunks && (c % cpr) == 0)
-            p.delta_t[t0 + static_cast<size_t>(c / cpr) * kBlockM] = v;
+            p.delta_t[t0 + static_cast<size_t>(c / cpr) * kBlockM] = -v;
         }
       }
     } else {
       for (int h = lane; h < p.hq; h += 32) {
         float v = 0.f;
         for (int c = 0; c < cpr; ++c) v += dot8<T>(o[h * cpr + c], g[h * cpr + c]);
-        p.delta_t[t0 + static_cast<size_t>(h) * kBlockM] = v;
+        p.delta_t[t0 + static_cast<size_t>(h) * kBlockM] = -v;
       }
     }
   }

@@ -53,8 +53,9 @@ struct Layout {
 //   q_pairs int2[cap_q]      sorted (sequence, query tile)
 //   k_pairs int2[cap_k]      sorted (sequence, key tile)
 //   f_pairs int2[cap_f]      sorted (sequence, 256-row query tile pair)
-//   lse_t   fp32[cap_q*hq*128] backward only: lse * log2(e), tile-major
-//   delta_t fp32[cap_q*hq*128] backward only: rowsum(dO * O), tile-major
+//   lse_t   fp32[cap_q*hq*128] backward only: -lse * log2(e), tile-major
+//   delta_t fp32[cap_q*hq*128] backward only: -rowsum(dO * O), tile-major (both
+//           negated so that the consumers add them without a negation)
 //   dq_acc  fp32[cap_q*hq*128*dq_cols] fused backward only: the ordered dQ
 //           accumulator, one 128-row tile per (query tile pair, head)
 //   dq_sem  int32[cap_q*hq]  fused backward only: key tiles added to each dQ tile
