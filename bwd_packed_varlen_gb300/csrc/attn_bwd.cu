@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
       constexpr uint32_t idAcc = make_idesc_f16(kBF16, false, true, 128, S::kDo);
       const uint32_t t_dk = tmem + S::kColDK, t_dv = tmem + S::kColDV;
@@ -240,10 +240,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SmemDesc ddo_mn = smem_desc(smem_u32(sDO), kBM * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      auto wait_q = [&](int cur) { return mbar_wait(&bar_q_full[cur % NS], (cur / NS) & 1, status); };
+      auto wait_q = [&](int cur) { return mbar_wait_warp(&bar_q_full[cur % NS], (cur / NS) & 1, status); };
       // S^T = K Q^T (A: K tile, B: Q stage) or dP^T = V dO^T for global step `cur`.
       auto issue_st = [&](int cur, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
         const SmemDesc bst{b.lo + ((cur % NS) * S::kQBytes >> 4), b.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s)
           mma_ss(d_tmem, a, (s >> 2) * 16384 + (s & 3) * 32, bst, (s >> 2) * (kBM * 128) + (s & 3) * 32,
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_acc = [&](int cur, uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t split_off,
                            uint32_t acc0) {
         const SmemDesc bst{b.lo + (((cur % NS) * S::kQBytes + split_off) >> 4), b.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kBM / 16; ++s)
           mma_ts(d_tmem, a_tmem + packed_col<kBM>(s), bst, s * 2048, idAcc, s > 0 ? 1u : acc0);
@@ -263,11 +265,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       } I;
       for (; ok; ++ii) {
         int aux = 0;
-        const int item = ring_get(ring, ii, status, &ok, &aux);
+        const int item = ring_get_warp_once(ring, ii, status, &ok, &aux);
         if (!ok || item < 0) break;
         I.steps = aux & 0xffffff;
         I.split = aux >> 24;
-        if (!(ok = mbar_wait(&bar_kv_full, ii & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&bar_kv_full, ii & 1, status))) break;
         const uint32_t split_off = I.split * (S::kDo / 64) * kBM * 128;
         if (!(ok = wait_q(it))) break;
         tc_fence_after();
@@ -279,8 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int t = 0; t < I.steps; ++t) {
           const int cur = it + t;
           const bool more = t + 1 < I.steps;
-          if (!(ok = mbar_wait(&bar_p_ready, cur & 1, status))) break;
-          if (t == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&bar_p_ready, cur & 1, status))) break;
+          if (t == 0 && ii > 0 && !(ok = mbar_wait_warp(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           issue_acc(cur, t_dv, t_st, ddo_mn, split_off, t > 0 ? 1u : 0u);
           if (NS >= 2 && more) {
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             issue_st(cur + 1, t_st, dk, dq, &bar_s_full);
           }
-          if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&bar_ds_ready, cur & 1, status))) break;
           tc_fence_after();
           issue_acc(cur, t_dk, t_dpt, dq_mn, split_off, t > 0 ? 1u : 0u);
           mma_commit(&bar_q_empty[cur % NS]);
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBN);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, false, true, 128, kD);
       const uint32_t t_dq = tmem + S::kColDQ, t_s = tmem + S::kColS, t_dp = tmem + S::kColDP;
@@ -630,11 +632,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const SmemDesc dk_mn = smem_desc(smem_u32(sK), kBN * 128, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      auto wait_k = [&](int cur) { return mbar_wait(&bar_k_full[cur % KS], (cur / KS) & 1, status); };
-      auto wait_v = [&](int cur) { return mbar_wait(&bar_v_full[cur % VS], (cur / VS) & 1, status); };
+      auto wait_k = [&](int cur) { return mbar_wait_warp(&bar_k_full[cur % KS], (cur / KS) & 1, status); };
+      auto wait_v = [&](int cur) { return mbar_wait_warp(&bar_v_full[cur % VS], (cur / VS) & 1, status); };
       // S = Q K^T (a = Q, b = K stage) or dP = dO V^T (a = dO, b = V stage).
       auto issue_s = [&](int stage, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
         const SmemDesc bst{b.lo + (stage * S::kKVBytes >> 4), b.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s2 = 0; s2 < kD / 16; ++s2)
           mma_ss(d_tmem, a, (s2 >> 2) * 16384 + (s2 & 3) * 32, bst, (s2 >> 2) * (kBN * 128) + (s2 & 3) * 32,
@@ -643,9 +646,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       for (; ok; ++ii) {
         int n = 0;
-        const int item = ring_get(ring, ii, status, &ok, &n);
+        const int item = ring_get_warp_once(ring, ii, status, &ok, &n);
         if (!ok || item < 0) break;
-        if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&bar_q_full, ii & 1, status))) break;
         if (!(ok = wait_k(it))) break;
         if (!(ok = wait_v(it))) break;
         tc_fence_after();
@@ -663,12 +666,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int cur = it + j;
           const bool more = j + 1 < n;
           if (kEarlyS && more) {
-            if (!(ok = mbar_wait(&bar_s_free, cur & 1, status))) break;
+            if (!(ok = mbar_wait_warp(&bar_s_free, cur & 1, status))) break;
             tc_fence_after();
             issue_s((cur + 1) % KS, t_s, dq, dk, &bar_s_full);
           }
-          if (!(ok = mbar_wait(&bar_ds_ready, cur & 1, status))) break;
-          if (j == 0 && ii > 0 && !(ok = mbar_wait(&bar_acc_empty, (ii - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&bar_ds_ready, cur & 1, status))) break;
+          if (j == 0 && ii > 0 && !(ok = mbar_wait_warp(&bar_acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           // Early-S order: dP_j+1 goes ahead of dQ_j (its region was read before
           // ds_ready_j), so the compute warps start on dS_j+1 while the tensor
@@ -677,6 +680,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const SmemDesc kst{dk_mn.lo + ((cur % KS) * S::kKVBytes >> 4), dk_mn.hi};
           const uint32_t a_ds = t_ds + (cur & 1) * S::kDsCols;
           const uint32_t acc0 = j > 0 ? 1u : 0u;
+          __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
           for (int s2 = 0; s2 < kBN / 16; ++s2)
             mma_ts(t_dq, a_ds + s2 * 8, kst, s2 * 2048, idDQ, s2 > 0 ? 1u : acc0);

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   } else if (warp == kFusedWarpMma) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBM);
       constexpr uint32_t idAcc = make_idesc_f16(kBF16, false, true, 128, kD);
       constexpr uint32_t idDQ = make_idesc_f16(kBF16, true, true, 128, kD);
@@ -287,10 +287,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const SmemDesc dk_mn = smem_desc(smem_u32(sK), 16384, 1024, kLayoutSW128);
       int it = 0, ii = 0;
       bool ok = true;
-      auto wait_q = [&](int cur) { return mbar_wait(&B.q_full[cur & 1], (cur >> 1) & 1, status); };
+      auto wait_q = [&](int cur) { return mbar_wait_warp(&B.q_full[cur & 1], (cur >> 1) & 1, status); };
       // S^T = K Q^T or dP^T = V dO^T of step `cur` (B from the step's stage).
       auto issue_st = [&](int cur, uint32_t d_tmem, SmemDesc a, SmemDesc b, uint64_t* done) {
         const SmemDesc bst{b.lo + (((cur & 1) * S::kTileBytes) >> 4), b.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s)
           mma_ss(d_tmem, a, (s >> 2) * 16384 + (s & 3) * 32, bst, (s >> 2) * 16384 + (s & 3) * 32, idS,
@@ -300,12 +301,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // dV += P^T dO (a_off 0) or dK += dS^T Q (a_off 16) of step `cur`.
       auto issue_acc = [&](int cur, uint32_t d_tmem, uint32_t a_off, SmemDesc b, uint32_t acc0) {
         const SmemDesc bst{b.lo + (((cur & 1) * S::kTileBytes) >> 4), b.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kBM / 16; ++s)
           mma_ts(d_tmem, t_x + a_off + fused_packed_col(s), bst, s * 2048, idAcc, s > 0 ? 1u : acc0);
       };
       // dQ_t = dS K into Y.
       auto issue_dq = [&]() {
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kBlockN / 16; ++s)
           mma_ss(t_y, dds_mn, s * 2048, dk_mn, s * 2048, idDQ, s > 0 ? 1u : 0u);
@@ -313,23 +316,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       };
       for (; ok; ++ii) {
         int steps = 0;
-        const int item = ring_get(B.ring, ii, status, &ok, &steps);
+        const int item = ring_get_warp_once(B.ring, ii, status, &ok, &steps);
         if (!ok || item < 0) break;
-        if (!(ok = mbar_wait(&B.kv_full, ii & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&B.kv_full, ii & 1, status))) break;
         if (!(ok = wait_q(it))) break;
         tc_fence_after();
         issue_st(it, t_x, dk, dq, &B.s_full);
         // Y holds the previous step's dQ until the compute warps have read it
-        if (it > 0 && !(ok = mbar_wait(&B.y_free, (it - 1) & 1, status))) break;
+        if (it > 0 && !(ok = mbar_wait_warp(&B.y_free, (it - 1) & 1, status))) break;
         tc_fence_after();
         issue_st(it, t_y, dv, ddo, &B.dp_full);
         for (int t = 0; t < steps; ++t) {
           const int cur = it + t;
-          if (!(ok = mbar_wait(&B.p_ready, cur & 1, status))) break;
-          if (t == 0 && ii > 0 && !(ok = mbar_wait(&B.acc_empty, (ii - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&B.p_ready, cur & 1, status))) break;
+          if (t == 0 && ii > 0 && !(ok = mbar_wait_warp(&B.acc_empty, (ii - 1) & 1, status))) break;
           tc_fence_after();
           issue_acc(cur, t_dv, 0, ddo_mn, t > 0 ? 1u : 0u);
-          if (!(ok = mbar_wait(&B.ds_ready, cur & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&B.ds_ready, cur & 1, status))) break;
           tc_fence_after();
           issue_acc(cur, t_dk, 16, dq_mn, t > 0 ? 1u : 0u);
           issue_dq();
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (!(ok = wait_q(cur + 1))) break;
           tc_fence_after();
           issue_st(cur + 1, t_x, dk, dq, &B.s_full);
-          if (!(ok = mbar_wait(&B.y_free, cur & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&B.y_free, cur & 1, status))) break;
           tc_fence_after();
           issue_st(cur + 1, t_y, dv, ddo, &B.dp_full);
         }

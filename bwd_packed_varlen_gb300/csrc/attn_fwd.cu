@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc_f16(kBF16, false, false, 128, kBlockN);
       constexpr uint32_t idPV = make_idesc_f16(kBF16, false, true, 128, kD);
       // Operand descriptors: Q and K K-major; V as the N-major (d-contiguous) B of P V.
@@ -156,10 +156,11 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       auto issue_s = [&](int t) -> bool {
         const int sk = t % SK;
-        if (!mbar_wait(&bar_k_full[sk], (t / SK) & 1, status)) return false;
+        if (!mbar_wait_warp(&bar_k_full[sk], (t / SK) & 1, status)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem + S::kColS0 + (t & 1) * kBlockN;
         const SmemDesc kst{dk.lo + ((sk * S::kTileBytes) >> 4), dk.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s) {
           const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(192, 1)
         const int n = (visible_keys(s, pr.y, causal) + kBlockN - 1) / kBlockN;
         if (n == 0) continue;
         const int k = ii++;  // index of this item among the block's processed ones
-        if (!(ok = mbar_wait(&bar_q_full, k & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&bar_q_full, k & 1, status))) break;
         if (!(ok = issue_s(it))) break;
         for (int j = 0; j < n && ok; ++j) {
           const int cur = it + j;
@@ -184,14 +185,15 @@ __global__ void __launch_bounds__(192, 1)
           } else {
             mma_commit(&bar_q_empty);
           }
-          if (!(ok = mbar_wait(&bar_p_ready[cur & 1], (cur >> 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&bar_p_ready[cur & 1], (cur >> 1) & 1, status))) break;
           const int sv = cur % SV;
-          if (!(ok = mbar_wait(&bar_v_full[sv], (cur / SV) & 1, status))) break;
-          if (j == 0 && k > 0 && !(ok = mbar_wait(&bar_o_empty, (k - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&bar_v_full[sv], (cur / SV) & 1, status))) break;
+          if (j == 0 && k > 0 && !(ok = mbar_wait_warp(&bar_o_empty, (k - 1) & 1, status))) break;
           tc_fence_after();
           const uint32_t a_tmem = tmem + S::kColS0 + (cur & 1) * kBlockN;
           const SmemDesc vst{dv.lo + ((sv * S::kTileBytes) >> 4), dv.hi};
           const uint32_t acc0 = j > 0 ? 1u : 0u;
+          __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
           for (int s = 0; s < kBlockN / 16; ++s)
             mma_ts(t_o, a_tmem + s * 8, vst, s * 2048, idPV, s > 0 ? 1u : acc0);

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
     }
   } else if (warp == kFwdWarpMma) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS =
           kFP8 ? make_idesc_e4m3(128, kBlockN) : make_idesc_f16(kBF16, false, false, 128, kBlockN);
       constexpr uint32_t idPV = make_idesc_f16(kBF16, false, true, 128, kD);
@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       auto issue_s = [&](int x, int st) {
         const SmemDesc qx{dq.lo + ((x * S::kQKBytes) >> 4), dq.hi};
         const SmemDesc kst{dk.lo + ((st * S::kQKBytes) >> 4), dk.hi};
+        __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
         for (int s = 0; s < S::kSKSteps; ++s) {
           // 32 bytes of K per MMA: 16 16-bit or 32 8-bit elements
@@ -219,13 +220,13 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       } I;
       for (int ii = 0; ok; ++ii) {
         int counts = 0;
-        const int item = ring_get(ring, ii, status, &ok, &counts);
+        const int item = ring_get_warp_once(ring, ii, status, &ok, &counts);
         if (!ok || item < 0) break;
         I.n[0] = counts & 0xffff;
         I.n[1] = counts >> 16;
         I.nmax = I.n[0] > I.n[1] ? I.n[0] : I.n[1];
-        if (!(ok = mbar_wait(&bar_q_full, ii & 1, status))) break;
-        if (!(ok = mbar_wait(&bar_k_full[it % NS], (it / NS) & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&bar_q_full, ii & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&bar_k_full[it % NS], (it / NS) & 1, status))) break;
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
           if (I.n[x] > 0) issue_s(x, it % NS);
@@ -236,16 +237,17 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
           bool v_ready = false, k_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
             if (j >= I.n[x]) continue;
-            if (!(ok = mbar_wait(&bar_p_ready[x], np[x] & 1, status))) break;
+            if (!(ok = mbar_wait_warp(&bar_p_ready[x], np[x] & 1, status))) break;
             ++np[x];
-            if (j == 0 && no[x] > 0 && !(ok = mbar_wait(&bar_o_empty[x], (no[x] - 1) & 1, status))) break;
+            if (j == 0 && no[x] > 0 && !(ok = mbar_wait_warp(&bar_o_empty[x], (no[x] - 1) & 1, status))) break;
             if (!v_ready) {
-              if (!(ok = mbar_wait(&bar_v_full[st], (cur / NS) & 1, status))) break;
+              if (!(ok = mbar_wait_warp(&bar_v_full[st], (cur / NS) & 1, status))) break;
               v_ready = true;
             }
             tc_fence_after();
             const SmemDesc vst{dv.lo + ((st * S::kVBytes) >> 4), dv.hi};
             const uint32_t acc0 = j > 0 ? 1u : 0u;
+            __syncwarp();  // elect.sync in the MMA wrappers needs a converged warp
 #pragma unroll
             for (int s = 0; s < kBlockN / 16; ++s)
               mma_ts(tmem + S::col_o(x), tmem + S::col_s(x) + s * 8, vst, s * 2048, idPV,
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
             if (j + 1 < I.n[x]) {
               const int nx = cur + 1;
               if (!k_ready) {
-                if (!(ok = mbar_wait(&bar_k_full[nx % NS], (nx / NS) & 1, status))) break;
+                if (!(ok = mbar_wait_warp(&bar_k_full[nx % NS], (nx / NS) & 1, status))) break;
                 k_ready = true;
               }
               tc_fence_after();

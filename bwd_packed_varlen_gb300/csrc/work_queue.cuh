@@ -63,6 +63,23 @@ __device__ __forceinline__ int ring_get_warp(WorkRing& r, int k, int* status, bo
   return item;
 }
 
+// Consumer (a whole warp, counted once in `consumers`): every lane waits and reads
+// the warp-uniform item; lane 0 alone arrives on the slot's empty barrier.
+__device__ __forceinline__ int ring_get_warp_once(WorkRing& r, int k, int* status, bool* ok,
+                                                  int* aux) {
+  const int s = k & 1;
+  if (!__all_sync(0xffffffffu, mbar_wait(&r.full[s], (k >> 1) & 1, status))) {
+    *ok = false;
+    return -1;
+  }
+  const int item = *reinterpret_cast<volatile int*>(&r.item[s]);
+  *aux = *reinterpret_cast<volatile int*>(&r.aux[s]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[s]);
+  __syncwarp();
+  return item;
+}
+
 // Producer: index of the block's next work item (the first is blockIdx.x).
 __device__ __forceinline__ int next_item(int* counter) {
   return static_cast<int>(gridDim.x) + atomicAdd(counter, 1);
