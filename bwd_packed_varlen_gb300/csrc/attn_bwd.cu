@@ -2,7 +2,8 @@
 //
 // Two persistent tensor-core kernels with the same role split: 16 compute warps
 // (warp w owns TMEM lane quarter w % 4 and a quarter of the step's columns), one
-// TMA producer warp and one warp whose lane 0 issues every tcgen05.mma. Work items
+// TMA producer warp and one MMA warp (the whole warp runs the issue loop; one
+// elected lane issues every tcgen05.mma). Work items
 // come from the scheduler's sorted lists through a per-kernel counter and a
 // shared-memory ring (see work_queue.cuh).
 //

@@ -38,8 +38,8 @@
 //
 // Roles (768 threads, six warpgroups): 16 compute warps (warp w owns TMEM lanes
 // 32*(w%4).. and query columns [32*(w/4), +32) of S^T and dP^T, output columns
-// [kD/4*(w/4), +kD/4) of dK and dV); a TMA producer warp; an MMA warp (lane 0 issues
-// every tcgen05.mma); two reducer warps (lane 0) that add the staged dQ tiles of
+// [kD/4*(w/4), +kD/4) of dK and dV); a TMA producer warp; an MMA warp (one elected
+// lane issues every tcgen05.mma); two reducer warps (lane 0) that add the staged dQ tiles of
 // even and odd steps to the accumulator with bulk reductions; and four drain warps
 // (one per TMEM lane quarter) that read dQ_t out of TMEM and stage it, so neither
 // the compute warps nor the MMA warp ever wait on dQ's way to global memory. dQ_t

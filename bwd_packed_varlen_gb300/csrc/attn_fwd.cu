@@ -9,7 +9,7 @@
 //   warp 4  (TMA)     loads the Q tile once per item and K/V tiles of 128 key
 //                     rows into multi-stage shared-memory rings (128-byte swizzle,
 //                     rows at the PADDED offsets, rows past the tensor read as 0);
-//   warp 5  (MMA)     one thread issues tcgen05 MMAs: S_j = Q K_j^T into one of two
+//   warp 5  (MMA)     one elected lane issues tcgen05 MMAs: S_j = Q K_j^T into one of two
 //                     TMEM score buffers, then O += P_j V_j with P_j read from TMEM;
 //   warps 0-3 (softmax) one thread per query row: masks by the REAL lengths
 //                     (key j visible iff j < Lk, and j <= i when causal), runs the

@@ -7,7 +7,7 @@
 //   warps 0-3  softmax of tile A (one thread per query row / TMEM lane),
 //   warps 4-7  softmax of tile B,
 //   warp 8     TMA producer (Q_A, Q_B once per item; K_j, V_j rings),
-//   warp 9     MMA issuer (lane 0).
+//   warp 9     MMA issuer (the whole warp; one elected lane issues).
 // TMEM: O_A [0, 128), O_B [128, 256), S_A [256, 384), S_B [384, 512). The issue
 // order is  S_A0, S_B0 | PV_A0, S_A1 | PV_B0, S_B1 | PV_A1, S_A2 | ...  so while one
 // softmax warpgroup turns S into P the tensor cores work on the other tile. Since
