@@ -27,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -180,11 +181,19 @@ KERNEL_SOURCES = {"fwd": ["attn_fwd_pair.cu"] + _HEADERS, "dkdv": ["attn_bwd.cu"
                   "dq": ["attn_bwd.cu"] + _HEADERS, "bwd_fused": ["attn_bwd_fused.cu"] + _HEADERS}
 
 
+def code_only(text):
+    """C++ source without comments and with whitespace collapsed: edits to comments
+    leave a kernel's hash (and so its traffic record) unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bwd_packed_varlen_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

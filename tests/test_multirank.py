@@ -69,3 +69,18 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.whole_job_tflops(5.0e12, 5.0, 1) == pytest.approx(1000.0)
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The traffic record stays valid across comment edits and goes stale on any
+    code edit: the hash covers the sources with comments and whitespace removed."""
+    sys.path.insert(0, ROOT)
+    import bench
+    code = "int f(int x) {  // doubles x\n  return 2 * x; /* no overflow check */\n}\n"
+    recommented = "// f: twice x\nint f(int x) {\n  return 2 * x;   // same code\n}\n"
+    changed = "int f(int x) {  // doubles x\n  return 3 * x;\n}\n"
+    assert bench.code_only(code) == bench.code_only(recommented)
+    assert bench.code_only(code) != bench.code_only(changed)
+    assert bench.code_only('asm("mov.b32 %0, %1;");') == 'asm("mov.b32 %0, %1;");'
+    for k in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_source_hash(k)) == 16
