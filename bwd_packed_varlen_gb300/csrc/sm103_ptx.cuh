@@ -27,14 +27,6 @@ __device__ __forceinline__ uint32_t lane_id() {
   return r;
 }
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
