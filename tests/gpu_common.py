@@ -7,6 +7,7 @@ import numpy as np
 import torch
 
 import oracle
+from bwd_packed_varlen_gb300 import workloads as W
 
 # Tolerances of the GPU path against the float64 oracle (bf16/fp16 inputs):
 # relative Frobenius error <= 1e-2 on out/dq/dk/dv, cosine >= 0.9999,
@@ -154,3 +155,19 @@ def check_against_oracle(w, res, ref=None):
     assert err <= LSE_TOL, f"lse: max abs err {err:.3e}"
     m["lse"] = float(err)
     return m
+
+
+def random_configs(n=16, seed=2026):
+    """Seeded draws over the supported parameter space: head dim any multiple of 8
+    in [8, 256], 1-4 query heads per kv head, every mask, both 16-bit types, 1-6
+    sequences of 0-350 rows with independent query and key lengths."""
+    rng = np.random.default_rng(seed)
+    masks = [W.MASK_PADDING, W.MASK_PADDING_CAUSAL, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT]
+    out = []
+    for i in range(n):
+        d = 8 * int(rng.integers(1, 33))
+        hkv = int(rng.choice([1, 2, 4]))
+        hq = hkv * int(rng.integers(1, 5))
+        out.append((100 + i, int(rng.integers(1, 7)), int(rng.integers(1, 351)), hq, hkv, d,
+                    masks[int(rng.integers(0, 3))], ["bf16", "fp16"][int(rng.integers(0, 2))]))
+    return out

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from bwd_packed_varlen_gb300 import workloads as W
-from gpu_common import check_against_oracle, gpu_fwd_bwd, to_dev
+from gpu_common import check_against_oracle, gpu_fwd_bwd, random_configs, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -153,3 +153,26 @@ def test_debug_build_fused_backward_and_e4m3_forward():
     for a, b in zip(tuple(release) + tuple(rel_e4) + tuple(two_kernel),
                     tuple(debug) + tuple(dbg_e4) + tuple(dbg_two)):
         assert torch.equal(_bits(a), _bits(b))
+
+
+@pytest.mark.parametrize("case", random_configs(), ids=lambda c: f"s{c[0]}_d{c[5]}_h{c[3]}x{c[4]}_m{c[6]}_{c[7]}")
+def test_debug_build_random_configurations(case):
+    """The seeded random configurations of the parity tests under the bounds checks:
+    no out-of-bounds offset, a clean status word, and the release build's bits."""
+    import bwd_packed_varlen_gb300 as ta
+    seed, batch, max_len, hq, hkv, d, mask, dtype = case
+    w = W.random_varlen(seed, batch, max_len, hq, hkv, d, mask, dtype)
+    t = to_dev(w)
+    Tq, hq, d = w.q.shape
+    Tk, hkv, _ = w.k.shape
+    release = gpu_fwd_bwd(w, t)
+    wsf = torch.empty(ta.fwd_workspace_size(w.batch, Tq, Tk, hq, hkv, d), dtype=torch.uint8,
+                      device="cuda")
+    wsb = torch.empty(ta.bwd_workspace_size(w.batch, Tq, Tk, hq, hkv, d), dtype=torch.uint8,
+                      device="cuda")
+    with ta.debug_build():
+        debug = gpu_fwd_bwd(w, t, fwd={"workspace": wsf}, bwd={"workspace": wsb})
+        assert ta.read_status(wsf) == 0 and ta.read_status(wsb) == 0
+    for a, b in zip(release, debug):
+        assert torch.equal(_bits(a), _bits(b))
+

@@ -24,6 +24,7 @@ from gpu_common import (
     gpu_fwd_bwd,
     np64,
     oracle_fwd_bwd,
+    random_configs,
     to_dev,
 )
 
@@ -142,23 +143,7 @@ def test_ragged_edge_cases(case):
     check_against_oracle(w, gpu_fwd_bwd(w))
 
 
-def _random_configs(n=16, seed=2026):
-    """Seeded draws over the supported parameter space: head dim any multiple of 8
-    in [8, 256], 1-4 query heads per kv head, every mask, both 16-bit types, 1-6
-    sequences of 0-350 rows with independent query and key lengths."""
-    rng = np.random.default_rng(seed)
-    masks = [W.MASK_PADDING, W.MASK_PADDING_CAUSAL, W.MASK_PADDING_CAUSAL_BOTTOM_RIGHT]
-    out = []
-    for i in range(n):
-        d = 8 * int(rng.integers(1, 33))
-        hkv = int(rng.choice([1, 2, 4]))
-        hq = hkv * int(rng.integers(1, 5))
-        out.append((100 + i, int(rng.integers(1, 7)), int(rng.integers(1, 351)), hq, hkv, d,
-                    masks[int(rng.integers(0, 3))], ["bf16", "fp16"][int(rng.integers(0, 2))]))
-    return out
-
-
-@pytest.mark.parametrize("case", _random_configs(), ids=lambda c: f"s{c[0]}_d{c[5]}_h{c[3]}x{c[4]}_m{c[6]}_{c[7]}")
+@pytest.mark.parametrize("case", random_configs(), ids=lambda c: f"s{c[0]}_d{c[5]}_h{c[3]}x{c[4]}_m{c[6]}_{c[7]}")
 def test_random_configurations(case):
     """Seeded random shapes beyond the hand-picked edge cases, each element checked
     against the oracle (forward and backward)."""
