@@ -15,7 +15,10 @@
 // softmax may rescale O_X as soon as S_X(j+1) is ready. P_X(j) is written as 16-bit
 // values over S_X(j) and read from TMEM by PV_X(j). The running max is rescaled
 // lazily (only when it grows by more than 2^8); masks use the REAL lengths and are
-// applied only on tiles that need them.
+// applied only on tiles that need them. A tile's normalized O rows go to a
+// shared-memory O tile and leave with TMA stores issued by one thread, so the
+// softmax warps do not wait for the global writes (tiles that reach past their
+// sequence's padded rows store row by row instead).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,7 +47,8 @@ struct FwdPairShape {
   static constexpr int kQKColsPerChunk = kFP8 ? 128 : 64;      // elements in 128 bytes
   static constexpr int kSKSteps = kFP8 ? kD / 32 : kD / 16;    // MMAs per S (32 bytes of K each)
   static constexpr int kStages = 2;                            // K and V rings
-  static constexpr int kSmemUsed = kQKBytes * (2 + kStages) + kVBytes * kStages + 1024;
+  static constexpr int kOBytes = kChunks * 16384;                // O tile staged for the TMA store
+  static constexpr int kSmemUsed = kQKBytes * (2 + kStages) + kVBytes * kStages + kOBytes + 1024;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
   // TMEM columns of O_x and S_x for tile x (0: A, 1: B)
   __device__ static constexpr uint32_t col_o(int x) { return static_cast<uint32_t>(x) * 128u; }
@@ -66,6 +70,7 @@ struct FwdItem {
   int h, g, u;
   int n[2];      // key tiles tile A / tile B visit (0: tile absent)
   int nmax;
+  bool whole[2];  // tile rows lie inside the sequence's padded rows (TMA store allowed)
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool causal) {
@@ -80,13 +85,19 @@ __device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool 
   I.n[0] = (visible_keys(I.s, ta, causal) + kBlockN - 1) / kBlockN;
   I.n[1] = tb * kBlockM < I.s.len_q ? (visible_keys(I.s, tb, causal) + kBlockN - 1) / kBlockN : 0;
   I.nmax = I.n[0] > I.n[1] ? I.n[0] : I.n[1];
+  // the store box may not reach into the next sequence's rows; sequence-major
+  // tensors keep every sequence in its own batch entry (the box is clipped there)
+  const int pad_q = p.sbhd ? p.total_q : p.cu_q_pad[pr.x + 1] - p.cu_q_pad[pr.x];
+  I.whole[0] = ta * kBlockM + kBlockM <= pad_q;
+  I.whole[1] = tb * kBlockM + kBlockM <= pad_q;
   return I;
 }
 
 template <int kD, bool kBF16, bool kFP8 = false>
 __global__ void __launch_bounds__(kFwdPairThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
-                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO) {
   using S = FwdPairShape<kD, kFP8>;
   static_assert(!kFP8 || kBF16, "the e4m3 forward writes bf16");
   constexpr int NS = S::kStages;
@@ -96,10 +107,12 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
   uint8_t* sQ = smem;                          // tile A then tile B
   uint8_t* sK = sQ + 2 * S::kQKBytes;         // NS stages
   uint8_t* sV = sK + NS * S::kQKBytes;         // NS stages
+  uint8_t* sO = sV + NS * S::kVBytes;         // one O tile, shared by both tiles in turn
 
   __shared__ uint64_t bar_q_full, bar_q_empty;
   __shared__ uint64_t bar_k_full[NS], bar_k_empty[NS], bar_v_full[NS], bar_v_empty[NS];
   __shared__ uint64_t bar_s_full[2], bar_p_ready[2], bar_o_full[2], bar_o_empty[2];
+  __shared__ uint64_t bar_stage, bar_ostage[2];  // O staging free / a tile's rows staged
   __shared__ WorkRing ring;
   __shared__ uint32_t tmem_slot;
 
@@ -124,6 +137,9 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       mbar_init(&bar_o_empty[x], 128);
     }
     ring_init(ring, 1 + 256);
+    mbar_init(&bar_stage, 1);
+    mbar_init(&bar_ostage[0], 128);
+    mbar_init(&bar_ostage[1], 128);
     fence_barrier_init();
   }
   if (warp == kFwdWarpMma) {
@@ -292,12 +308,23 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       int item, n, lim;
       bool row_valid;
       size_t out_row;  // token * hq + head of this row
+      int stage_before;  // staging uses of this item before this tile's (0 or 1)
+      int stage_item;    // staging uses of this item (both tiles)
+      bool tma;          // this tile's O leaves through the staged TMA store
+      int h, tb, tok0;   // store coordinates of this tile
     };
     auto decode = [&](int item) {
-      RowItem r{item, 0, 0, false, 0};
+      RowItem r{item, 0, 0, false, 0, 0, 0, false, 0, 0, 0};
       if (item < 0) return r;
       const FwdItem I = fwd_item(p, item, causal);
       r.n = I.n[x];
+      const bool ua = I.n[0] > 0 && I.whole[0], ub = I.n[1] > 0 && I.whole[1];
+      r.tma = x == 0 ? ua : ub;
+      r.stage_before = x == 1 && ua ? 1 : 0;
+      r.stage_item = (ua ? 1 : 0) + (ub ? 1 : 0);
+      r.h = I.h;
+      r.tb = I.s.tb;
+      r.tok0 = I.s.off_q + (2 * I.u + x) * kBlockM;
       const int row = (2 * I.u + x) * kBlockM + quarter * 32 + lane;
       // rows that see no key (before a lower-right triangle) are the zero fill's
       r.lim = row < I.s.len_q ? row_keys(I.s, row, causal) : 0;
@@ -306,9 +333,11 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
                     bounds_ok(r.out_row < static_cast<size_t>(p.total_q) * p.hq, p.header + kHdrStatus);
       return r;
     };
+    int stage_uses = 0, ostage_uses = 0;  // O staging uses so far (block / this tile)
     RowItem cur = decode(ring_get_warp(ring, 0, status, &ok));
     for (int ii = 0; ok && cur.item >= 0; ++ii) {
       if (cur.n == 0) {
+        stage_uses += cur.stage_item;
         cur = decode(ring_get_warp(ring, ii + 1, status, &ok));
         continue;
       }
@@ -424,22 +453,68 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
       ++no;
       tc_fence_after();
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      const auto rows = make_row_pair(static_cast<T*>(p.out) + cur.out_row * static_cast<size_t>(p.d), row_valid);
+      if (cur.tma) {
+        // The tile's rows go to a shared-memory O tile (128-byte swizzle, as the TMA
+        // loads lay out Q) and leave with one TMA store per 64 columns, issued by one
+        // thread; the warps go on as soon as their rows are in shared memory. The
+        // buffer serves the block's tiles in turn: use u waits for use u-1's store
+        // to have read it.
+        const int u = stage_uses + cur.stage_before;
+        if (u > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_stage, (u - 1) & 1, status));
+        if (!ok) break;
+        const int r = quarter * 32 + lane;
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c0, o);
-        tmem_ld_wait();
-        store_pair16<kBF16>(rows, c0, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[0]), inv);
-        store_pair16<kBF16>(rows, c0 + 16, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[16]), inv);
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c0, o);
+          tmem_ld_wait();
+          uint8_t* row = sO + (c0 / 64) * 16384 + r * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int piece = ((c0 % 64) / 8) + v;
+            st_shared_v4(row + ((piece ^ (r & 7)) << 4),
+                         pack2<kBF16>(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                         pack2<kBF16>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                         pack2<kBF16>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                         pack2<kBF16>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_o_empty[x]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_ostage[x]);
+        if (quarter == 0 && lane == 0) {
+          // every row of the tile is in shared memory: store, wait for the reads, release
+          if (mbar_wait(&bar_ostage[x], ostage_uses & 1, status)) {
+#pragma unroll
+            for (int c = 0; c < S::kChunks; ++c) tma_store_4d(&tmO, sO + c * 16384, c * 64, cur.h, cur.tb, cur.tok0);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar_stage);
+        }
+        ++ostage_uses;
+      } else {
+        const auto rows = make_row_pair(static_cast<T*>(p.out) + cur.out_row * static_cast<size_t>(p.d), row_valid);
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c0, o);
+          tmem_ld_wait();
+          store_pair16<kBF16>(rows, c0, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[0]), inv);
+          store_pair16<kBF16>(rows, c0 + 16, p.d, *reinterpret_cast<uint32_t(*)[16]>(&o[16]), inv);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_o_empty[x]);
       }
       if (row_valid) p.lse[cur.out_row] = m * 0.69314718055994531f + logf(l);
-      tc_fence_before();
-      mbar_arrive(&bar_o_empty[x]);
+      stage_uses += cur.stage_item;
       cur = nxt;
     }
   }
 
+  // the stores' global writes are complete before the block ends
+  if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kFwdWarpMma) {
@@ -452,13 +527,14 @@ __global__ void __launch_bounds__(kFwdPairThreads, 1)
 template <int kD, bool kBF16, bool kFP8 = false>
 static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaStream_t st) {
   using S = FwdPairShape<kD, kFP8>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int nb = p.sbhd ? p.batch : 1;
   const bool qk_ok = kFP8 ? make_tmap_tokens_u8(&tq, p.q, p.total_q, nb, p.hq, p.d) &&
                                 make_tmap_tokens_u8(&tk, p.k, p.total_kv, nb, p.hkv, p.d)
                           : make_tmap_tokens(&tq, p.q, p.total_q, nb, p.hq, p.d, kBF16) &&
                                 make_tmap_tokens(&tk, p.k, p.total_kv, nb, p.hkv, p.d, kBF16);
-  if (!qk_ok || !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16))
+  if (!qk_ok || !make_tmap_tokens(&tv, p.v, p.total_kv, nb, p.hkv, p.d, kBF16) ||
+      !make_tmap_tokens(&to, p.out, p.total_q, nb, p.hq, p.d, kBF16))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_pair_kernel<kD, kBF16, kFP8>;
   cudaError_t e =
@@ -466,7 +542,7 @@ static cudaError_t launch_fwd_pair_impl(const AttnParams& p, int num_sms, cudaSt
   if (e != cudaSuccess) return e;
   const long long max_items = static_cast<long long>(p.pair_cap_f) * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? (max_items > 0 ? max_items : 1) : num_sms);
-  kern<<<grid, kFwdPairThreads, S::kSmemBytes, st>>>(p, tq, tk, tv);
+  kern<<<grid, kFwdPairThreads, S::kSmemBytes, st>>>(p, tq, tk, tv, to);
   return cudaGetLastError();
 }
 
