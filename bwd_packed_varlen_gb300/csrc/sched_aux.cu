@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -284,31 +285,15 @@ cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, int* 
 }
 
 // ---------------------------------------------------------------------------
-// Row classification shared by the zero fill and the preprocess
+// Zero fill: the rows no tile writes. Of sequence b's query rows these are a
+// prefix of real queries that see no key (all of them without keys; before the
+// lower-right triangle otherwise) and the pad rows after its real ones; of its key
+// rows, those no real query sees and the pad rows. Block (b, y) clears a share of
+// sequence b's rows, one warp per row with 16-byte stores; block b = batch clears
+// the packed rows outside every sequence. Rows are kept inside the tensors even
+// when the lengths are inconsistent (the scheduler reports those).
 // ---------------------------------------------------------------------------
-// 0: not computed; 1: computed by a tensor-core kernel; 2: real query that sees
-// no key (its sequence has none, or the lower-right triangle starts after it).
-__device__ __forceinline__ int q_row_kind(const AttnParams& p, int r) {
-  int i = 0;
-  const int b = locate_row(p, p.cu_q_pad, r, &i);
-  if (b < 0) return 0;
-  SeqInfo s = load_seq(p, b);
-  if (i >= s.len_q) return 0;
-  return row_keys(s, i, p.causal) > 0 ? 1 : 2;
-}
-
-__device__ __forceinline__ bool k_row_computed(const AttnParams& p, int r) {
-  int j = 0;
-  const int b = locate_row(p, p.cu_kv_pad, r, &j);
-  if (b < 0) return false;
-  SeqInfo s = load_seq(p, b);
-  return j < seen_keys(s, p.causal);
-}
-
-// ---------------------------------------------------------------------------
-// Zero fill: one warp per row, 16-byte stores.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void zero_row(void* base, int r, int row_bytes) {
+__device__ __forceinline__ void zero_row(void* base, long long r, int row_bytes) {
   uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(base) +
                                         static_cast<size_t>(r) * row_bytes);
   const uint4 z = make_uint4(0, 0, 0, 0);
@@ -317,39 +302,70 @@ __device__ __forceinline__ void zero_row(void* base, int r, int row_bytes) {
 
 // mode 0: forward (out, lse); mode 1: backward (dq, dk, dv)
 __global__ void __launch_bounds__(256) zero_fill_kernel(AttnParams p, int mode) {
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  const int nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+  const int w0 = blockIdx.y * nw + (threadIdx.x >> 5), wstep = nw * gridDim.y;
   const int qbytes = p.hq * p.d * 2, kbytes = p.hkv * p.d * 2;
-  for (int r = gw; r < p.total_q; r += warps) {
-    int kind = q_row_kind(p, r);
-    if (kind == 1) continue;
+  const bool causal = p.causal != 0;
+  // query row r: out / lse (v on the lse) or dq
+  auto clear_q = [&](long long r, float v) {
+    if (r < 0 || r >= p.total_q) return;
     if (mode == 0) {
       zero_row(p.out, r, qbytes);
-      float v = kind == 2 ? -INFINITY : 0.0f;
       for (int h = lane; h < p.hq; h += 32) p.lse[static_cast<size_t>(r) * p.hq + h] = v;
     } else {
       zero_row(p.dq, r, qbytes);
     }
+  };
+  auto clear_k = [&](long long r) {
+    if (r < 0 || r >= p.total_kv) return;
+    zero_row(p.dk, r, kbytes);
+    zero_row(p.dv, r, kbytes);
+  };
+  if (b < p.batch) {
+    const SeqInfo s = load_seq(p, b);
+    // rows of sequence b: base + i * stride for i in [0, n)
+    const long long qbase = p.sbhd ? b : p.cu_q_pad[b];
+    const int qn = min(max(p.sbhd ? p.total_q / p.batch : p.cu_q_pad[b + 1] - p.cu_q_pad[b], 0), p.total_q);
+    const int stride = p.sbhd ? p.batch : 1;
+    const int dead = s.len_k == 0 ? s.len_q : (causal ? min(s.len_q, max(0, -s.diag)) : 0);
+    const int nq = dead + max(0, qn - s.len_q);
+    for (int z = w0; z < nq; z += wstep) {
+      const int i = z < dead ? z : s.len_q + (z - dead);
+      clear_q(qbase + static_cast<long long>(i) * stride, z < dead ? -INFINITY : 0.0f);
+    }
+    if (mode == 1) {
+      const long long kbase = p.sbhd ? b : p.cu_kv_pad[b];
+      const int kn = min(max(p.sbhd ? p.total_kv / p.batch : p.cu_kv_pad[b + 1] - p.cu_kv_pad[b], 0), p.total_kv);
+      const int seen = seen_keys(s, causal);
+      for (int j = seen + w0; j < kn; j += wstep) clear_k(kbase + static_cast<long long>(j) * stride);
+    }
+  } else if (!p.sbhd) {
+    // packed rows before the first and after the last sequence: [0, lo) and [hi, total)
+    auto outside = [&](int first, int last, int total, auto&& clear) {
+      const int lo = min(max(first, 0), total), hi = min(max(last, lo), total);
+      const int n = lo + (total - hi);
+      for (int z = w0; z < n; z += wstep) clear(z < lo ? z : hi + (z - lo));
+    };
+    outside(p.cu_q_pad[0], p.cu_q_pad[p.batch], p.total_q, [&](long long r) { clear_q(r, 0.0f); });
+    if (mode == 1) outside(p.cu_kv_pad[0], p.cu_kv_pad[p.batch], p.total_kv, clear_k);
   }
-  if (mode == 1) {
-    for (int r = gw; r < p.total_kv; r += warps) {
-      if (k_row_computed(p, r)) continue;
-      zero_row(p.dk, r, kbytes);
-      zero_row(p.dv, r, kbytes);
-    }
-    // fused backward: the per-(query tile, head) counters of key tiles added to dQ
-    if (p.dq_sem) {
-      const size_t n = static_cast<size_t>(p.pair_cap_q) * p.hq;
-      const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-      for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
-        p.dq_sem[i] = 0;
-    }
+  // fused backward: the per-(query tile, head) counters of key tiles added to dQ
+  if (mode == 1 && p.dq_sem) {
+    const size_t n = static_cast<size_t>(p.pair_cap_q) * p.hq;
+    const size_t nb = static_cast<size_t>(gridDim.x) * gridDim.y;
+    const size_t stride = nb * blockDim.x;
+    const size_t bid = static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    for (size_t i = bid * blockDim.x + threadIdx.x; i < n; i += stride) p.dq_sem[i] = 0;
   }
 }
 
 cudaError_t launch_zero_fill(const AttnParams& p, int mode, int num_sms, cudaStream_t st) {
-  zero_fill_kernel<<<num_sms * 4, 256, 0, st>>>(p, mode);
+  // one block per sequence plus one for the rows outside them, repeated along y
+  // so that about four blocks per SM share the rows of few long sequences
+  const int nb = p.batch + 1;
+  const int y = std::max(1, std::min(65535, (num_sms * 4 + nb - 1) / nb));
+  zero_fill_kernel<<<dim3(nb, y), 256, 0, st>>>(p, mode);
   return cudaGetLastError();
 }
 
