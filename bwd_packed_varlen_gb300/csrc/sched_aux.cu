@@ -144,55 +144,111 @@ __device__ void build_chain_list(const AttnParams& p, const int* pref, int n, in
   __syncthreads();
 }
 
-// kKind: 0 query tiles, 1 key tiles, 2 forward pairs of query tiles.
+// kKind: 0 query tiles, 1 key tiles, 2 forward pairs of query tiles. The sort of
+// a list of n <= kSortCap pairs runs in three phases, each over the threads
+// [t, t + nt): the keys (cost descending, then list position) padded to a power of
+// two m, the bitonic stages (k, j), and the sorted pairs written out.
+template <int kKind>
+__device__ void list_keys(const AttnParams& p, const int* pref, int n, int m, uint64_t* keys, int t,
+                          int nt) {
+  for (int i = t; i < m; i += nt) {
+    uint64_t key = ~0ull;
+    if (i < n) {
+      const int b = find_seq(pref, p.batch, i);
+      const int tt = i - pref[b];
+      const int cost = kKind == 0 ? q_pair_cost(p, b, tt)
+                       : (kKind == 1 ? k_pair_cost(p, b, tt) : f_pair_cost(p, b, tt));
+      key = (static_cast<uint64_t>(0x7fffffffu - static_cast<uint32_t>(cost)) << 32) |
+            static_cast<uint32_t>(i);
+    }
+    keys[i] = key;
+  }
+}
+
+__device__ __forceinline__ void list_stage(uint64_t* keys, int m, int k, int j, int t, int nt) {
+  for (int i = t; i < m; i += nt) {
+    const int ixj = i ^ j;
+    if (ixj > i) {
+      const uint64_t a = keys[i], c = keys[ixj];
+      const bool up = (i & k) == 0;
+      if ((a > c) == up) {
+        keys[i] = c;
+        keys[ixj] = a;
+      }
+    }
+  }
+}
+
+__device__ void list_out(const AttnParams& p, const int* pref, int n, int2* out, const uint64_t* keys,
+                         int t, int nt) {
+  for (int i = t; i < n; i += nt) {
+    const int src = static_cast<int>(keys[i] & 0xffffffffu);
+    const int b = find_seq(pref, p.batch, src);
+    out[i] = make_int2(b, src - pref[b]);
+  }
+}
+
+__device__ __forceinline__ int pow2_at_least(int n) {
+  int m = 1;
+  while (m < n) m <<= 1;
+  return m;
+}
+
 template <int kKind>
 __device__ void build_list(const AttnParams& p, const int* pref, int n, int2* out,
                            uint64_t* keys) {
-  const int B = p.batch;
   if (n <= kSortCap) {
-    int m = 1;
-    while (m < n) m <<= 1;
-    for (int i = threadIdx.x; i < m; i += blockDim.x) {
-      uint64_t key = ~0ull;
-      if (i < n) {
-        int b = find_seq(pref, B, i);
-        int t = i - pref[b];
-        int cost = kKind == 0 ? q_pair_cost(p, b, t)
-                   : (kKind == 1 ? k_pair_cost(p, b, t) : f_pair_cost(p, b, t));
-        key = (static_cast<uint64_t>(0x7fffffffu - static_cast<uint32_t>(cost)) << 32) |
-              static_cast<uint32_t>(i);
-      }
-      keys[i] = key;
-    }
+    const int m = pow2_at_least(n);
+    list_keys<kKind>(p, pref, n, m, keys, threadIdx.x, blockDim.x);
     __syncthreads();
     for (int k = 2; k <= m; k <<= 1) {
       for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < m; i += blockDim.x) {
-          int ixj = i ^ j;
-          if (ixj > i) {
-            uint64_t a = keys[i], c = keys[ixj];
-            bool up = (i & k) == 0;
-            if ((a > c) == up) {
-              keys[i] = c;
-              keys[ixj] = a;
-            }
-          }
-        }
+        list_stage(keys, m, k, j, threadIdx.x, blockDim.x);
         __syncthreads();
       }
     }
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      int src = static_cast<int>(keys[i] & 0xffffffffu);
-      int b = find_seq(pref, B, src);
-      out[i] = make_int2(b, src - pref[b]);
-    }
+    list_out(p, pref, n, out, keys, threadIdx.x, blockDim.x);
     __syncthreads();
   } else {
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      int b = find_seq(pref, B, i);
+      int b = find_seq(pref, p.batch, i);
       out[i] = make_int2(b, i - pref[b]);
     }
   }
+}
+
+// The backward's query-tile and key-tile lists, sorted side by side: half of the
+// threads each, one block-wide barrier per stage of the longer list (the shorter
+// list's stages are a prefix of it), so the two sorts cost about one.
+__device__ void build_q_k_lists(const AttnParams& p, const int* pref_q, int nq, const int* pref_k, int nk,
+                                uint64_t* keys) {
+  const int half = blockDim.x / 2;
+  const bool first = threadIdx.x < half;
+  const int t = first ? threadIdx.x : threadIdx.x - half;
+  uint64_t* kq = keys;
+  uint64_t* kk = keys + kSortCap;
+  const int mq = pow2_at_least(nq), mk = pow2_at_least(nk);
+  if (first)
+    list_keys<0>(p, pref_q, nq, mq, kq, t, half);
+  else
+    list_keys<1>(p, pref_k, nk, mk, kk, t, half);
+  __syncthreads();
+  const int mmax = mq > mk ? mq : mk;
+  for (int k = 2; k <= mmax; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (first) {
+        if (k <= mq) list_stage(kq, mq, k, j, t, half);
+      } else {
+        if (k <= mk) list_stage(kk, mk, k, j, t, half);
+      }
+      __syncthreads();
+    }
+  }
+  if (first)
+    list_out(p, pref_q, nq, p.q_pairs, kq, t, half);
+  else
+    list_out(p, pref_k, nk, p.k_pairs, kk, t, half);
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, int* pref_q,
@@ -238,9 +294,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
   const int nq = min(carry_q, p.pair_cap_q);
   const int nk = min(carry_k, p.pair_cap_k);
   const int nf = min(carry_f, p.pair_cap_f);
-  if (p.sched_lists & kListQ) build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
-  if (p.sched_lists & kListK) build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
-  else if (p.sched_lists & kListKChain) {
+  const bool both = (p.sched_lists & kListQ) && (p.sched_lists & kListK) && nq <= kSortCap &&
+                    nk <= kSortCap;
+  if (both) {
+    build_q_k_lists(p, pref_q, nq, pref_k, nk, sort_keys);
+  } else {
+    if (p.sched_lists & kListQ) build_list<0>(p, pref_q, nq, p.q_pairs, sort_keys);
+    if (p.sched_lists & kListK) build_list<1>(p, pref_k, nk, p.k_pairs, sort_keys);
+  }
+  if (!(p.sched_lists & kListK) && (p.sched_lists & kListKChain)) {
     build_chain_list(p, pref_k, nk, p.k_pairs, sort_keys);
     __syncthreads();
     // Items of the fused backward, chain-major: sequence b's pairs occupy list
@@ -275,7 +337,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(AttnParams p, i
 
 cudaError_t launch_schedule(const AttnParams& p, int* pref_q, int* pref_k, int* pref_f,
                             cudaStream_t st) {
-  const size_t smem = kSortCap * sizeof(uint64_t);
+  const size_t smem = 2 * kSortCap * sizeof(uint64_t);  // two lists sorted side by side
   cudaError_t e = cudaFuncSetAttribute(schedule_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
