@@ -38,6 +38,10 @@
  *   sees no key (its sequence has no real key, or it precedes a lower-right
  *   causal triangle) gets out = 0, lse = -inf, dq = 0.
  *   Pad slots may hold any finite values; they never reach a real output.
+ *   q, k, v, out, dout, dq, dk and dv must start on a 16-byte boundary (tiles are
+ *   moved with 16-byte vector and bulk-tensor copies); a pointer that does not is
+ *   answered with TE_ERR_INVALID_ARG before anything is launched. lse and the
+ *   cu_seqlens arrays need their natural 4-byte alignment.
  *
  * Supported: d a multiple of 8 with 8 <= d <= 256; hq a positive multiple of hkv;
  *   mask TE_MASK_PADDING, TE_MASK_PADDING_CAUSAL (key j visible to query i iff

@@ -149,6 +149,28 @@ def test_host_checked_errors_launch_nothing(lib):
                                 None) == -1       # rows overflow int
 
 
+def test_misaligned_tensor_pointers_are_refused(lib):
+    """A tensor pointer off a 16-byte boundary is answered with TE_ERR_INVALID_ARG
+    before any launch, on the forward and on every backward tensor (placeholder
+    pointers that the library never dereferences on this path)."""
+    import ctypes
+    P = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    cu = ctypes.c_void_p(1 << 21)
+    big = ctypes.c_size_t(1 << 40)
+    args = (cu, cu, cu, cu, 2, 64, 64, 0, 0, 4, 2, 64, 0.1, 1, 1, P, big, None)
+    for i in (0, 1, 2, 3):                        # q, k, v, out
+        ptrs = [P] * 5
+        ptrs[i] = bad
+        assert lib.te_attn_fwd_thd(*ptrs, *args) == -1, i
+        assert b"aligned" in lib.te_attn_last_error()
+    for i in (0, 1, 2, 3, 4, 6, 7, 8):            # q, k, v, out, dout, dq, dk, dv
+        ptrs = [P] * 9
+        ptrs[i] = bad
+        assert lib.te_attn_bwd_thd(*ptrs, *args) == -1, i
+        assert b"aligned" in lib.te_attn_last_error()
+
+
 def test_debug_build_exports_the_same_symbols(lib):
     """The bounds-checking build exports every declared function too."""
     import bwd_packed_varlen_gb300 as ta
