@@ -53,12 +53,17 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["throughput", "small"], default="throughput",
                     help="small: the same recipe with 8192 real tokens (for ncu captures)")
+    ap.add_argument("--head-dim", type=int, default=128,
+                    help="head dim of the workload (a multiple of 8 in [8, 256]; default 128)")
     ap.add_argument("--bwd", choices=["two-kernel", "fused"], default="two-kernel",
                     help="backward of the timed step: te_attn_bwd_thd (dQ and dK/dV kernels) "
                          "or te_attn_bwd_thd_fused (one pass)")
     ap.add_argument("--configs", action="store_true",
                     help="time every configuration beside the CPU oracle (one line each)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if not (8 <= args.head_dim <= 256 and args.head_dim % 8 == 0):
+        ap.error("--head-dim must be a multiple of 8 in [8, 256]")
+    return args
 
 
 # ----------------------------------------------------------------- helpers
@@ -322,7 +327,7 @@ def measure_variants(ta, w, t, flops, fwd_flops, flush, dev, steps=20, warmup=5)
     out = {}
     f8 = getattr(torch, "float8_e4m3fn", None)
     cu = (t["cu_seqlens_q"], t["cu_seqlens_kv"], t["cu_seqlens_q_padded"], t["cu_seqlens_kv_padded"])
-    if f8 is not None:
+    if f8 is not None and w.d % 16 == 0 and w.d <= 128:  # the e4m3 forward's head dims
         def quant(x):
             descale = float(x.float().abs().amax()) / 448.0
             return (x.float() / descale).clamp(-448.0, 448.0).to(f8), descale
@@ -392,8 +397,9 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from bwd_packed_varlen_gb300 import workloads as W
-    w = W.throughput()
-    seqs, groups = [4], [0]
+    w = (W.throughput(d=args.head_dim) if args.workload == "throughput"
+         else W.throughput(total=8192, d=args.head_dim))
+    seqs, groups = [min(4, w.batch - 1)], [0]
     for _ in range(args.warmup):
         oracle_sample(w, seqs, groups)
     times, fl = [], 0.0
@@ -402,8 +408,9 @@ def run_reference(args, rank, world):
         times.append(t)
     mean = sum(times) / len(times)
     val = fl / mean / 1e12
-    sample = (f"sequence 4 ({int(w.cu_seqlens_q[5] - w.cu_seqlens_q[4])} tokens) x kv-group 0 "
-              f"(4 query heads) of the workload, fwd+bwd")
+    b = seqs[0]
+    sample = (f"sequence {b} ({int(w.cu_seqlens_q[b + 1] - w.cu_seqlens_q[b])} tokens) x kv-group 0 "
+              f"({w.hq // w.hkv} query heads) of the workload, fwd+bwd")
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
@@ -425,7 +432,10 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     ta.library()
-    w = W.throughput() if args.workload == "throughput" else W.throughput(total=8192)
+    w = (W.throughput(d=args.head_dim) if args.workload == "throughput"
+         else W.throughput(total=8192, d=args.head_dim))
+    # the committed DRAM counts were taken on the default workload only
+    default_workload = args.workload == "throughput" and args.head_dim == 128
     flops = w.algorithmic_flops()
     pairs_h = causal_pairs(w) * w.hq  # sum over (sequence, query head) of Lq*Lk/2
     t = {k: getattr(w, k).to(dev) for k in ("q", "k", "v", "dout", "cu_seqlens_q",
@@ -630,7 +640,8 @@ def run_ours(args, rank, world, local_rank):
     peak = peaks["bf16_tflops"]
     ach = kernels[dom]["tflops_credited"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": ncu_traffic(dom),
+                "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": ncu_traffic(dom) if default_workload else None,
                 "peak_kind": f"bf16 dense burst ({peaks['source']})",
                 "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                 "flops_per_launch": credited[dom]}
