@@ -215,16 +215,21 @@ __device__ __forceinline__ PairHead item_pair_head(int item, int n_pairs, int he
 // head 0, then head 1, ...). Whole-list group-major order would start the last
 // groups' longest key tiles late and leave SMs idle at the end of the kernel; the
 // bands keep the list's longest-first order at band granularity while items of
-// one kv head still run side by side. `heads`: kv heads x column splits.
+// one kv head still run side by side. The last full band and the remainder go
+// pair-major instead (every head of a pair, pairs longest first), so the final
+// items the blocks take are the shortest ones and the blocks finish together.
+// `heads`: kv heads x column splits.
 __device__ __forceinline__ PairHead item_pair_head_banded(int item, int n_pairs, int heads) {
   constexpr int kBand = 64;
-  const int full = n_pairs / kBand, in_full = full * kBand * heads;
-  if (item < in_full) {
+  const int full = n_pairs / kBand;
+  const int banded_pairs = (full > 0 ? full - 1 : 0) * kBand;
+  const int banded_items = banded_pairs * heads;
+  if (item < banded_items) {
     const int c = item / (kBand * heads), r = item - c * (kBand * heads);
     return PairHead{c * kBand + r % kBand, r / kBand};
   }
-  const int last = n_pairs - full * kBand, r = item - in_full;
-  return PairHead{full * kBand + r % last, r / last};
+  const int r = item - banded_items;
+  return PairHead{banded_pairs + r / heads, r % heads};
 }
 
 // Number of key rows a query tile can see (the keys its last real row sees).

@@ -249,8 +249,10 @@ def test_running_max_raised_between_key_tiles(d, dtype, mask):
                          ids=["64_key_tiles", "65_key_tiles", "131_key_tiles"])
 def test_key_tile_list_band_boundaries(lengths):
     """dK/dV items come in bands of 64 sorted key tiles (kv-head-major inside a
-    band): exactly one full band, one full band plus one tile, and two full bands
-    plus three tiles must each cover every (key tile, kv head) once."""
+    band), except the last full band and the remainder, which go pair-major: exactly
+    one full band (all pair-major), one full band plus one tile (all pair-major), and
+    two full bands plus three tiles (one band, then 67 tiles pair-major) must each
+    cover every (key tile, kv head) once."""
     rng = np.random.default_rng(len(lengths))
     T, hq, hkv, d = sum(lengths), 4, 2, 32
     q, k, v, do = (torch.from_numpy(rng.standard_normal((T, h, d), dtype=np.float32)).to(torch.bfloat16)
