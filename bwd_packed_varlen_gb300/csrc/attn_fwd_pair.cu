@@ -73,9 +73,14 @@ struct FwdItem {
   bool whole[2];  // tile rows lie inside the sequence's padded rows (TMA store allowed)
 };
 
+// Items are numbered pair-major: every query head of a pair before the next pair,
+// pairs in list order (longest first). The blocks' last items are then the list's
+// shortest, so they finish together, and a pair's heads share one sequence's K/V
+// rows, which stay in L2 while they run. (The kernels with one query tile per item
+// keep the group-major order of item_pair_head, which measured faster for them.)
 __device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int item, bool causal) {
   FwdItem I;
-  const PairHead ph = item_pair_head(item, p.header[kHdrNumFPairs], p.group);
+  const PairHead ph{item / p.hq, item % p.hq};
   const int2 pr = p.f_pairs[ph.pair];
   I.h = ph.head;
   I.g = I.h / p.group;

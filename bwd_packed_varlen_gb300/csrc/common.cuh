@@ -195,7 +195,8 @@ __device__ __forceinline__ int row_keys(const SeqInfo& s, int i, bool causal) {
   return causal ? min(s.len_k, max(0, i + 1 + s.diag)) : s.len_k;
 }
 
-// Work items of the per-head kernels are numbered group-major: all items of kv
+// Work items of the dQ kernel and the one-tile forward are numbered group-major
+// (the two-tile forward numbers its own pair-major): all items of kv
 // head group 0, then group 1, ...; within a group the pairs in list order (longest
 // first) with the group's heads innermost. Blocks running at the same time then
 // work on one group's heads, whose Q/dO and K/V tiles stay in L2, rather than on
