@@ -84,3 +84,17 @@ def test_kernel_source_hash_ignores_comments_only():
     assert bench.code_only('asm("mov.b32 %0, %1;");') == 'asm("mov.b32 %0, %1;");'
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16
+
+
+def test_head_dim_option_is_checked(monkeypatch):
+    """`--head-dim` takes the library's head dims only (multiples of 8 in [8, 256]);
+    anything else stops at argument parsing, before any workload is built."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for good in ("8", "64", "256"):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--head-dim", good])
+        assert bench.parse().head_dim == int(good)
+    for bad in ("0", "12", "264"):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--head-dim", bad])
+        with pytest.raises(SystemExit):
+            bench.parse()
